@@ -1,0 +1,425 @@
+/*
+ * CPU oracle for the routed-expert forward of a Kimi K2 MoE block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the GPU library computes.  Only the test-suite, the
+ * package smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * Every floating-point value is carried in fp64 (C double).  Inputs are read
+ * from the exact bytes the GPU path reads: bf16 activations as raw 16-bit
+ * patterns, FP8 e4m3 weight codes as bytes, fp32 block scales and fp32 router
+ * weights.
+ *
+ * Sources (Kimi K2 model pages, pinned revision of modeling_deepseek.py and
+ * config.json):
+ *   - "Input features" page, FP8 quantisation config: weights are e4m3 with
+ *     one scale per 128 x 128 block; dequantised weight = code value x scale.
+ *   - "SwiGLU output" page, SwiGLU MLP class: expert(x) = down(silu(gate x) * up x),
+ *     three bias-free linears; gate/up map d -> d_ff, down maps d_ff -> d.
+ *   - "Element-wise product" page: h = a (.) u with a = silu(gate x).
+ *   - "Mixture of experts" page, moe_infer: count tokens per expert, sort the
+ *     flattened (token, slot) positions by expert, run each expert on its
+ *     contiguous slice, scatter the outputs back to their positions, then
+ *     sum each token's k outputs weighted by topk_weight.  The page's prose:
+ *     each token's output is the router-weighted sum of its selected experts
+ *     plus the shared expert applied to every token.
+ *   - "Input features" page, RMSNorm excerpt: y = gain * h / sqrt(mean(h^2) + eps);
+ *     decoder block: hidden = residual + mlp(post_attention_norm(residual)).
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *   - sort order of equal expert ids: ascending flat index t*k + j (stable);
+ *   - counting: a histogram that adds (a token naming one expert twice is
+ *     counted twice);
+ *   - the activation is SiLU, silu(a) = a / (1 + exp(-a));
+ *   - no intermediate rounding to bf16 anywhere (the exact function; any
+ *     rounding an implementation does is covered by the parity tolerance);
+ *   - summation order: ((sum over j ascending of w_j * E_j(x)) + shared(x)) + residual.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* OCP 8-bit floating point, E4M3: 1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits.  Exponent field 0 is subnormal: (m / 8) * 2^-6.  Otherwise
+ * (1 + m / 8) * 2^(e - 7).  S.1111.111 is NaN; there are no infinities, so
+ * S.1111.110 = 448 is the largest finite magnitude. */
+double oracle_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32 pattern. */
+double oracle_bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double g_e4m3[256];
+static pthread_once_t g_once = PTHREAD_ONCE_INIT;
+
+static void init_tables(void)
+{
+    for (int c = 0; c < 256; ++c)
+        g_e4m3[c] = oracle_e4m3_value((uint8_t)c);
+}
+
+/* One quantised weight matrix [rows, cols] of e4m3 codes with fp32 scales
+ * [rows/128, cols/128].  Element (r, c) dequantises to code(r, c) * scale(r/128, c/128). */
+typedef struct {
+    const uint8_t *q;
+    const float *s;
+    int64_t rows, cols;
+} qmat;
+
+static inline double wq(const qmat *m, int64_t r, int64_t c)
+{
+    return g_e4m3[m->q[r * m->cols + c]] * (double)m->s[(r / 128) * (m->cols / 128) + c / 128];
+}
+
+/* Dequantised element, exported so tests can compare it with a library routine. */
+double oracle_dequant(const uint8_t *q, const float *s, int64_t rows, int64_t cols, int64_t r, int64_t c)
+{
+    pthread_once(&g_once, init_tables);
+    qmat m = {q, s, rows, cols};
+    return wq(&m, r, c);
+}
+
+double oracle_silu(double a)
+{
+    return a / (1.0 + exp(-a));
+}
+
+/* ------------------------------------------------------------------------- */
+/* One SwiGLU expert on one input row                                        */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    qmat gate, up, down;   /* gate/up: [d_ff, d], down: [d, d_ff] */
+} expert_t;
+
+/* out[d] = down( silu(gate x) * (up x) ); scratch holds 3 * d_ff doubles. */
+static void expert_row(const expert_t *ex, int64_t d, int64_t dff, const double *x, double *out, double *scratch)
+{
+    double *g = scratch, *u = scratch + dff, *h = scratch + 2 * dff;
+    for (int64_t f = 0; f < dff; ++f) {
+        double a = 0.0, b = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            a += wq(&ex->gate, f, c) * x[c];
+            b += wq(&ex->up, f, c) * x[c];
+        }
+        g[f] = a;
+        u[f] = b;
+    }
+    for (int64_t f = 0; f < dff; ++f)
+        h[f] = oracle_silu(g[f]) * u[f];
+    for (int64_t r = 0; r < d; ++r) {
+        double acc = 0.0;
+        for (int64_t f = 0; f < dff; ++f)
+            acc += wq(&ex->down, r, f) * h[f];
+        out[r] = acc;
+    }
+}
+
+static expert_t make_expert(const uint8_t *const *wg, const float *const *sg, const uint8_t *const *wu,
+                            const float *const *su, const uint8_t *const *wd, const float *const *sd,
+                            int64_t e, int64_t d, int64_t dff)
+{
+    expert_t ex;
+    ex.gate = (qmat){wg[e], sg[e], dff, d};
+    ex.up = (qmat){wu[e], su[e], dff, d};
+    ex.down = (qmat){wd[e], sd[e], d, dff};
+    return ex;
+}
+
+/* Single expert on a batch of rows, for pins against a library matmul. */
+void oracle_expert_forward(int64_t n_rows, int64_t d, int64_t dff, const double *x, const uint8_t *wg,
+                           const float *sg, const uint8_t *wu, const float *su, const uint8_t *wd,
+                           const float *sd, double *out)
+{
+    pthread_once(&g_once, init_tables);
+    expert_t ex = {{wg, sg, dff, d}, {wu, su, dff, d}, {wd, sd, d, dff}};
+    double *scratch = (double *)malloc(sizeof(double) * 3 * dff);
+    for (int64_t i = 0; i < n_rows; ++i)
+        expert_row(&ex, d, dff, x + i * d, out + i * d, scratch);
+    free(scratch);
+}
+
+/* ------------------------------------------------------------------------- */
+/* RMSNorm                                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* xn = gain * h / sqrt(mean(h^2) + eps), one row. */
+static void rmsnorm_row(int64_t d, const uint16_t *h_bf16, const uint16_t *gain_bf16, double eps, double *xn)
+{
+    double ss = 0.0;
+    for (int64_t c = 0; c < d; ++c) {
+        double v = oracle_bf16_value(h_bf16[c]);
+        ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / (double)d + eps);
+    for (int64_t c = 0; c < d; ++c)
+        xn[c] = oracle_bf16_value(gain_bf16[c]) * (oracle_bf16_value(h_bf16[c]) * inv);
+}
+
+void oracle_rmsnorm(int64_t n, int64_t d, const uint16_t *h_bf16, const uint16_t *gain_bf16, double eps, double *xn)
+{
+    for (int64_t t = 0; t < n; ++t)
+        rmsnorm_row(d, h_bf16 + t * d, gain_bf16, eps, xn + t * d);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Routing plan: histogram, exclusive scan, stable order by expert           */
+/* ------------------------------------------------------------------------- */
+
+/* counts[E], offsets[E+1], sorted_pos[n*k], inv_pos[n*k].
+ * sorted_pos[i] = flat index (t*k + j) of the i-th entry when entries are
+ * ordered by (expert id, flat index).  inv_pos[p] = i with sorted_pos[i] = p.
+ * Entries whose id lies outside [0, E) are left out: inv_pos = -1 and the tail
+ * of sorted_pos beyond offsets[E] is -1.  Returns the number of such entries. */
+int64_t oracle_permute(int64_t n, int64_t k, int64_t E, const int32_t *ids, int32_t *counts, int32_t *offsets,
+                       int32_t *sorted_pos, int32_t *inv_pos)
+{
+    int64_t R = n * k, bad = 0;
+    for (int64_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t p = 0; p < R; ++p) {
+        if (ids[p] >= 0 && ids[p] < E)
+            counts[ids[p]] += 1;
+        else
+            bad += 1;
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int64_t e = 0; e < E; ++e)
+        next[e] = offsets[e];
+    for (int64_t p = 0; p < R; ++p) {
+        int32_t e = ids[p];
+        if (e >= 0 && e < E) {
+            sorted_pos[next[e]] = (int32_t)p;
+            inv_pos[p] = next[e];
+            next[e] += 1;
+        } else {
+            inv_pos[p] = -1;
+        }
+    }
+    for (int64_t i = offsets[E]; i < R; ++i)
+        sorted_pos[i] = -1;
+    free(next);
+    return bad;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Routed forward, token by token (brute force)                              */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int64_t d, dff, k, E;
+    const uint16_t *x;            /* [N, d] bf16: expert input rows */
+    const int32_t *ids;           /* [N, k] */
+    const float *w;               /* [N, k] */
+    const uint8_t *const *wg, *const *wu, *const *wd;   /* per-expert pointers (NULL if unused) */
+    const float *const *sg, *const *su, *const *sd;
+    /* full block only */
+    const uint16_t *resid;        /* [N, d] bf16 residual, or NULL */
+    const uint16_t *gain;         /* [d] bf16: x is the residual, normalised first */
+    double eps;
+    const uint8_t *shg, *shu, *shd;  /* shared expert, or NULL */
+    const float *ssg, *ssu, *ssd;
+    int64_t dff_sh;
+    /* work */
+    const int64_t *tok;           /* token indices to evaluate */
+    int64_t n_tok;
+    double *y;                    /* [n_tok, d] */
+    int64_t next;                 /* shared work counter */
+    pthread_mutex_t mu;
+} job_t;
+
+static int64_t take(job_t *jb)
+{
+    pthread_mutex_lock(&jb->mu);
+    int64_t i = jb->next++;
+    pthread_mutex_unlock(&jb->mu);
+    return i;
+}
+
+static void *token_worker(void *arg)
+{
+    job_t *jb = (job_t *)arg;
+    int64_t d = jb->d, dff = jb->dff, k = jb->k;
+    int64_t smax = dff > jb->dff_sh ? dff : jb->dff_sh;
+    double *xin = (double *)malloc(sizeof(double) * d);
+    double *o = (double *)malloc(sizeof(double) * d);
+    double *scratch = (double *)malloc(sizeof(double) * 3 * (smax > 0 ? smax : 1));
+    for (;;) {
+        int64_t i = take(jb);
+        if (i >= jb->n_tok)
+            break;
+        int64_t t = jb->tok[i];
+        double *acc = jb->y + i * d;
+        if (jb->gain)
+            rmsnorm_row(d, jb->x + t * d, jb->gain, jb->eps, xin);
+        else
+            for (int64_t c = 0; c < d; ++c)
+                xin[c] = oracle_bf16_value(jb->x[t * d + c]);
+        for (int64_t c = 0; c < d; ++c)
+            acc[c] = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            int32_t e = jb->ids[t * k + j];
+            if (e < 0 || e >= jb->E)
+                continue;
+            expert_t ex = make_expert(jb->wg, jb->sg, jb->wu, jb->su, jb->wd, jb->sd, e, d, dff);
+            expert_row(&ex, d, dff, xin, o, scratch);
+            double wt = (double)jb->w[t * k + j];
+            for (int64_t c = 0; c < d; ++c)
+                acc[c] += wt * o[c];
+        }
+        if (jb->shg) {
+            expert_t sh = {{jb->shg, jb->ssg, jb->dff_sh, d}, {jb->shu, jb->ssu, jb->dff_sh, d},
+                           {jb->shd, jb->ssd, d, jb->dff_sh}};
+            expert_row(&sh, d, jb->dff_sh, xin, o, scratch);
+            for (int64_t c = 0; c < d; ++c)
+                acc[c] += o[c];
+        }
+        if (jb->resid)
+            for (int64_t c = 0; c < d; ++c)
+                acc[c] += oracle_bf16_value(jb->resid[t * d + c]);
+    }
+    free(xin);
+    free(o);
+    free(scratch);
+    return NULL;
+}
+
+static void run_job(job_t *jb, int nthreads)
+{
+    pthread_once(&g_once, init_tables);
+    if (nthreads < 1)
+        nthreads = 1;
+    jb->next = 0;
+    pthread_mutex_init(&jb->mu, NULL);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_create(&th[i], NULL, token_worker, jb);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&jb->mu);
+}
+
+/* y[i, :] = sum_j topk_weight[t, j] * expert_{ids[t, j]}(x[t, :]) for t = tok[i].
+ * Expert pointer tables are indexed by expert id; entries of experts that
+ * no selected token uses may be NULL. */
+void oracle_moe_infer(int64_t d, int64_t dff, int64_t k, int64_t E, const uint16_t *x, const int32_t *ids,
+                      const float *w, const uint8_t *const *wg, const float *const *sg, const uint8_t *const *wu,
+                      const float *const *su, const uint8_t *const *wd, const float *const *sd,
+                      const int64_t *tok, int64_t n_tok, double *y, int nthreads)
+{
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.d = d; jb.dff = dff; jb.k = k; jb.E = E;
+    jb.x = x; jb.ids = ids; jb.w = w;
+    jb.wg = wg; jb.sg = sg; jb.wu = wu; jb.su = su; jb.wd = wd; jb.sd = sd;
+    jb.tok = tok; jb.n_tok = n_tok; jb.y = y;
+    run_job(&jb, nthreads);
+}
+
+/* Full block for the selected tokens:
+ * y = h + ( sum_j w_j * E_j(xn) + S(xn) ),  xn = RMSNorm(h) with gain and eps.
+ * The shared expert pointers may be NULL (no shared expert). */
+void oracle_layer_forward(int64_t d, int64_t dff, int64_t k, int64_t E, const uint16_t *hidden,
+                          const uint16_t *gain, double eps, const int32_t *ids, const float *w,
+                          const uint8_t *const *wg, const float *const *sg, const uint8_t *const *wu,
+                          const float *const *su, const uint8_t *const *wd, const float *const *sd,
+                          const uint8_t *shg, const float *ssg, const uint8_t *shu, const float *ssu,
+                          const uint8_t *shd, const float *ssd, int64_t dff_sh, const int64_t *tok,
+                          int64_t n_tok, double *y, int nthreads)
+{
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.d = d; jb.dff = dff; jb.k = k; jb.E = E;
+    jb.x = hidden; jb.ids = ids; jb.w = w;
+    jb.wg = wg; jb.sg = sg; jb.wu = wu; jb.su = su; jb.wd = wd; jb.sd = sd;
+    jb.resid = hidden; jb.gain = gain; jb.eps = eps;
+    jb.shg = shg; jb.shu = shu; jb.shd = shd; jb.ssg = ssg; jb.ssu = ssu; jb.ssd = ssd;
+    jb.dff_sh = shg ? dff_sh : 0;
+    jb.tok = tok; jb.n_tok = n_tok; jb.y = y;
+    run_job(&jb, nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Routed forward the way the "Mixture of experts" page's moe_infer does it  */
+/* ------------------------------------------------------------------------- */
+
+/* Sorted-slice form: count, sort the flat positions by expert, gather the
+ * token rows into that order, run each expert on its contiguous slice, write
+ * each output row back to its flat position, then sum each token's k rows
+ * weighted by topk_weight.  Used on small inputs to pin oracle_moe_infer:
+ * the per-row arithmetic and the summation order are the same, so the two
+ * must agree bit for bit.  y is [n, d]. */
+void oracle_moe_infer_sorted(int64_t n, int64_t d, int64_t dff, int64_t k, int64_t E, const uint16_t *x,
+                             const int32_t *ids, const float *w, const uint8_t *const *wg,
+                             const float *const *sg, const uint8_t *const *wu, const float *const *su,
+                             const uint8_t *const *wd, const float *const *sd, double *y)
+{
+    pthread_once(&g_once, init_tables);
+    int64_t R = n * k;
+    int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    int32_t *idxs = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
+    int32_t *inv = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
+    oracle_permute(n, k, E, ids, counts, offsets, idxs, inv);
+    double *sorted_tokens = (double *)malloc(sizeof(double) * (size_t)(R * d));
+    double *outs = (double *)malloc(sizeof(double) * (size_t)(R * d));
+    double *new_x = (double *)calloc((size_t)(R * d), sizeof(double));
+    double *scratch = (double *)malloc(sizeof(double) * 3 * dff);
+    int64_t nvalid = offsets[E];
+    for (int64_t i = 0; i < nvalid; ++i) {
+        int64_t t = idxs[i] / k;
+        for (int64_t c = 0; c < d; ++c)
+            sorted_tokens[i * d + c] = oracle_bf16_value(x[t * d + c]);
+    }
+    int64_t start = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        int64_t end = start + counts[e];
+        if (counts[e] == 0)
+            continue;
+        expert_t ex = make_expert(wg, sg, wu, su, wd, sd, e, d, dff);
+        for (int64_t i = start; i < end; ++i)
+            expert_row(&ex, d, dff, sorted_tokens + i * d, outs + i * d, scratch);
+        start = end;
+    }
+    for (int64_t i = 0; i < nvalid; ++i)
+        memcpy(new_x + (int64_t)idxs[i] * d, outs + i * d, sizeof(double) * (size_t)d);
+    for (int64_t t = 0; t < n; ++t) {
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < k; ++j)
+                acc += (double)w[t * k + j] * new_x[(t * k + j) * d + c];
+            y[t * d + c] = acc;
+        }
+    }
+    free(counts); free(offsets); free(idxs); free(inv);
+    free(sorted_tokens); free(outs); free(new_x); free(scratch);
+}
