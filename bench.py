@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-expert forward of a Kimi K2 MoE block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k2_decode] [--impl ours|reference]
+
+One step = one pass of the whole path on one batch of synthetic input:
+routing plan (histogram + stable permutation), sorted-row gather, gate/up
+grouped GEMM with SwiGLU, down grouped GEMM with router weighting and
+scatter, ordered combine (plus RMSNorm, shared expert and residual for the
+full-block workload).  Inputs and all 384 experts' FP8 weights are resident
+in HBM before the timed region; the touched weights of one step (>= 4.8 GB)
+are far larger than L2, so no flush is needed.
+
+Multi-GPU: the path is data-parallel over tokens (replicated weights, no
+exchange), so each rank runs its own batch (weak scaling) and the job value is
+all ranks' tokens / the slowest rank's time.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "K2 MoE-layer tokens/s; % of HBM (decode) / FP8 tensor (prefill) roofline"
+
+
+def _peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return None
+
+
+def _hbm_peak():
+    p = _peaks()
+    if p and p.get("hbm_gbs"):
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _bf16_peak(sustained):
+    p = _peaks()
+    if p:
+        k = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        if p.get(k):
+            return float(p[k]), "measured"
+    return (1700.0 if sustained else 1900.0), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- algorithmic cost
+
+def algorithmic(wl, ids_list, n_tokens):
+    """Bytes and flops one step must move / do (touched experts only; intermediates excluded)."""
+    import torch
+    d, dff = wl.d, wl.d_ff
+    per_proj = d * dff + (d // 128) * (dff // 128) * 4          # e4m3 codes + fp32 block scales
+    touched = sum(int(torch.unique(ids).numel()) for ids in ids_list)
+    R = n_tokens * wl.top_k
+    gateup_bytes = touched * 2 * per_proj + R * d * 2 + R * dff * 2   # weights + sorted rows in + h out
+    down_bytes = touched * per_proj + R * dff * 2 + R * d * 2           # weights + h in + weighted rows out
+    step_bytes = touched * 3 * per_proj + n_tokens * d * 2 * (2 if not wl.full_block else 3) + n_tokens * 8 * wl.top_k
+    flops = 6 * d * dff * R
+    if wl.full_block:
+        step_bytes += 3 * (d * wl.d_ff_shared + (d // 128) * (wl.d_ff_shared // 128) * 4)
+        flops += 6 * d * wl.d_ff_shared * n_tokens
+    return {"touched_experts": touched, "gateup_bytes": gateup_bytes, "down_bytes": down_bytes,
+            "step_bytes": step_bytes, "step_flops": flops}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_ffn_infer_gb300 as mx
+    from mixture_experts_ffn_infer_gb300 import synthetic as syn
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = syn.WORKLOADS[args.workload]
+    mx.load_library()
+    # each rank its own batch (seed offset by rank), the same resident weights
+    rank_wl = syn.Workload(**{**wl.__dict__, "seed": wl.seed + 1000 * rank})
+    x, ids, w, gain = syn.make_host_inputs(rank_wl)
+    bank = syn.expert_bank(wl.num_experts, wl.d, wl.d_ff, syn.bank_seed_of(wl), dev)
+    shared = syn.expert_bank(1, wl.d, wl.d_ff_shared, wl.seed + 1_000_003, dev) if wl.full_block else None
+    n = x.shape[0]
+    xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
+    gaind = gain.to(dev) if gain is not None else None
+    dm = mx.dims(wl.d, wl.d_ff, wl.num_experts, wl.top_k)
+    dff_sh = wl.d_ff_shared if wl.full_block else 0
+    ws = mx.workspace(dm, n, dff_sh, dev)
+    out = torch.empty(n, wl.d, dtype=torch.bfloat16, device=dev)
+    W = mx.weights(bank)
+    WS = mx.weights(shared) if shared is not None else None
+    stream = torch.cuda.current_stream(dev)
+
+    n_ev = 12
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    traces = []
+    for k in range(args.steps):
+        t = mx.moe_trace()
+        for i, e in enumerate(evs[k]):
+            e.record(stream)  # materialise the event handle
+            t.events[i] = e.cuda_event
+        t.n_events = n_ev
+        traces.append(t)
+    torch.cuda.synchronize(dev)
+
+    def step(trace=None, xin=xd, idin=idsd, win=wd, o=out):
+        if wl.full_block:
+            mx.moe_layer_forward(dm, n, xin, gaind, 1e-6, idin, win, W, WS, dff_sh, o, ws, stream=stream,
+                                 trace=trace)
+        else:
+            mx.moe_infer(dm, n, xin, idin, win, W, o, ws, stream=stream, trace=trace)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = mx.moe_get_error(ws, stream)
+    if st != mx.MOE_OK:
+        raise RuntimeError(f"device error after warm-up: {mx.STATUS.get(st)}")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(traces[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+
+    # per-kernel durations from the trace events of every timed step
+    per_kernel = {}
+    launches = 0
+    for k in range(args.steps):
+        t = traces[k]
+        nrec = t.n_recorded
+        launches += nrec - 1
+        for i in range(nrec - 1):
+            lab = t.labels[i].decode()
+            per_kernel.setdefault(lab, []).append(evs[k][i].elapsed_time(evs[k][i + 1]))
+    kern_ms = {k: statistics.mean(v) for k, v in per_kernel.items()}
+
+    # end to end through the same C ABI with host buffers: pinned H2D of the step's inputs,
+    # the call, D2H of the result, every step inside the timed region
+    xh, idh, wh = x.pin_memory(), ids.pin_memory(), w.pin_memory()
+    oh = torch.empty(n, wl.d, dtype=torch.bfloat16).pin_memory()
+    xe, ide, we = torch.empty_like(xd), torch.empty_like(idsd), torch.empty_like(wd)
+    oe = torch.empty_like(out)
+
+    def e2e_step():
+        xe.copy_(xh, non_blocking=True)
+        ide.copy_(idh, non_blocking=True)
+        we.copy_(wh, non_blocking=True)
+        step(None, xe, ide, we, oe)
+        oh.copy_(oe, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    st = mx.moe_get_error(ws, stream)
+    if st != mx.MOE_OK:
+        raise RuntimeError(f"device error in the timed region: {mx.STATUS.get(st)}")
+
+    alg = algorithmic(wl, [ids], n)
+    ms_step = ms_total / args.steps
+    tokens = n * world
+    value = tokens * args.steps / (ms_total / 1e3)
+    hbm, hbm_src = _hbm_peak()
+    dominant = "gateup_swiglu"
+    dom_ms = kern_ms.get(dominant)
+    achieved = alg["gateup_bytes"] / (dom_ms / 1e3) / 1e9 if dom_ms else None
+    step_roof_ms = alg["step_bytes"] / (hbm * 1e9) * 1e3
+    bf16, bf16_src = _bf16_peak(sustained=True)
+    tflops = alg["step_flops"] / (ms_step / 1e3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get(dominant)
+        except (OSError, ValueError):
+            traffic = None
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
+                   "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
+                   "full_block": wl.full_block, "weights": "e4m3, fp32 scale per 128x128 block",
+                   "touched_experts": alg["touched_experts"],
+                   "l2": "inputs larger than L2: %.2f GB of touched expert weights per step" % (
+                       alg["step_bytes"] / 1e9),
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
+                     "peak_source": hbm_src + " (MEASURED_PEAKS.json hbm_gbs)" if hbm_src == "measured" else hbm_src,
+                     "unit": "GB/s", "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
+                     "alg_bytes_per_launch": alg["gateup_bytes"], "kernel_ms": dom_ms},
+        "step_roofline": {"bytes": alg["step_bytes"], "flops": alg["step_flops"], "t_roof_ms_hbm": step_roof_ms,
+                          "frac_hbm": step_roof_ms / ms_step, "tflops": tflops,
+                          "frac_bf16_sustained": tflops / bf16, "bf16_peak_source": bf16_src},
+        "kernel_ms": kern_ms,
+        "e2e": {"value": tokens * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x.numel() * 2 + ids.numel() * 4 + w.numel() * 4),
+                "d2h_bytes_per_step": int(n * wl.d * 2), "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=args.cpu_budget)
+    return result
+
+
+def _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s):
+    """Time the oracle on a token sample; returns (tokens/s, tokens, seconds, threads)."""
+    import oracle
+    import torch
+    tokens = list(range(n_tok))
+    used = torch.unique(ids[:n_tok]).tolist()
+    bank_h = _HostBank(bank, used)          # experts the sample touches, copied to host before timing
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    if wl.full_block:
+        oracle.layer_forward(x, gain, 1e-6, ids, w, bank_h, _HostBank(shared, [0]), tokens=tokens, threads=threads)
+    else:
+        oracle.moe_infer(x, ids, w, bank_h, tokens=tokens, threads=threads)
+    dt = time.perf_counter() - t0
+    return n_tok / dt, n_tok, dt, threads
+
+
+class _HostBank:
+    """Host copies of the listed experts, indexable like the device bank (others absent)."""
+
+    def __init__(self, bank, experts):
+        for nm in ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down"):
+            full = getattr(bank, nm)
+            setattr(self, nm, _Sparse(full, experts))
+
+
+class _Sparse:
+    def __init__(self, full, experts):
+        self.shape = tuple(full.shape)
+        self.rows = {int(e): full[int(e)].to("cpu") for e in experts}
+
+    def __getitem__(self, e):
+        return self.rows[int(e)]
+
+
+def cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=20.0):
+    # sample: the first tokens of the batch; one probe token sizes the sample to the budget
+    rate1, _, dt1, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, 1, budget_s)
+    n_tok = max(1, min(x.shape[0], int(budget_s / max(dt1, 1e-3) * max(1, threads // 2))))
+    rate, n_tok, dt, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s)
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_tok} of {x.shape[0]} tokens of the {wl.name} batch (fp64 C oracle, "
+                      f"one thread per token), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args):
+    import torch
+
+    from mixture_experts_ffn_infer_gb300 import synthetic as syn
+    wl = syn.WORKLOADS[args.workload]
+    x, ids, w, gain = syn.make_host_inputs(wl)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    bank = syn.expert_bank(wl.num_experts, wl.d, wl.d_ff, syn.bank_seed_of(wl), dev)
+    shared = syn.expert_bank(1, wl.d, wl.d_ff_shared, wl.seed + 1_000_003, dev) if wl.full_block else None
+    import oracle
+    threads = oracle.default_threads()
+    per_step = max(1, min(x.shape[0], args.ref_tokens_per_step))
+    times = []
+    for s in range(args.warmup + args.steps):
+        lo = (s * per_step) % x.shape[0]
+        tok = [(lo + i) % x.shape[0] for i in range(per_step)]
+        used = torch.unique(ids[tok]).tolist()
+        hb = _HostBank(bank, used)
+        t0 = time.perf_counter()
+        if wl.full_block:
+            oracle.layer_forward(x, gain, 1e-6, ids, w, hb, _HostBank(shared, [0]), tokens=tok, threads=threads)
+        else:
+            oracle.moe_infer(x, ids, w, hb, tokens=tok, threads=threads)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = per_step * len(times) / total
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "n_tokens_per_gpu": x.shape[0], "d": wl.d, "d_ff": wl.d_ff,
+                   "num_experts": wl.num_experts, "top_k": wl.top_k},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} tokens of the {wl.name} batch per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="k2_decode",
+                    choices=["tiny", "k2_decode", "k2_prefill", "k2_skewed", "k2_block"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-tokens-per-step", type=int, default=2)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * moe_ffn.h - C ABI of the GB300 routed-expert forward of a Kimi K2 MoE block.
+ *
+ * The operation (Kimi K2 model pages, pinned modeling_deepseek.py):
+ *   "Mixture of experts" page, moe_infer: given token features x [n, d],
+ *   router output topk_ids / topk_weight [n, k] and E SwiGLU experts, count
+ *   the tokens of each expert, sort the flattened (token, slot) positions by
+ *   expert, run every expert on its contiguous slice, put each output row
+ *   back at its position and sum each token's k rows weighted by topk_weight.
+ *   "SwiGLU output" page, MLP class: expert(x) = down(silu(gate x) * up x).
+ *   "Element-wise product" page: h = silu(gate x) (.) (up x), [.., d_ff].
+ *   "Input features" page, quantisation config: each linear weight is FP8
+ *   e4m3 with one fp32 scale per 128 x 128 block (weight = code * scale).
+ *   "Input features" page, decoder block + RMSNorm: the MoE block computes
+ *   hidden + moe(RMSNorm(hidden)), RMSNorm(h) = gain * h / sqrt(mean(h^2) + eps)
+ *   in fp32; "Mixture of experts" page, forward: plus one shared expert
+ *   applied to every token.
+ *
+ * Conventions shared by every entry point
+ *   - Buffers: all pointers except the dims/weights structs are DEVICE
+ *     pointers owned by the caller.  The library never allocates or frees
+ *     device memory and keeps no state between calls; scratch lives in the
+ *     caller's workspace (see moe_workspace_size).
+ *   - Layouts are dense row-major.  Sizes: n tokens, d model width, d_ff
+ *     expert width, E experts, k experts per token, R = n * k routed rows.
+ *   - Types: activations bf16 (uint16 bit patterns), expert rows f16,
+ *     router ids int32, router weights fp32, weights e4m3 bytes + fp32 scales.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream),
+ *     performs no host synchronisation and can run inside stream capture.
+ *     Errors that the host can see are returned at once and nothing is
+ *     launched.  Errors only the device can see (an expert id outside
+ *     [0, E), a duplicate id within one token when validation is on, a
+ *     bounded wait that gave up, a value outside the f16 range) set a word in
+ *     the workspace; the offending rows are skipped, never read or written
+ *     out of bounds; moe_get_error reports and clears the word.
+ *   - n = 0 is a no-op that returns MOE_OK.  Experts that no token selects
+ *     cost nothing (they are skipped, as the page's loop skips them).
+ *   - Limits: d and d_ff multiples of 128, 1 <= E <= 1024, 1 <= k <= 32,
+ *     n * k < 2^31.  Pointers handed to the tensor-memory-access engine
+ *     (weights, x) must be 16-byte aligned; the workspace 256-byte aligned.
+ *
+ * Precision: the expert GEMMs multiply f16 operands (the e4m3 weight codes
+ * and the bf16 activations both convert to f16 exactly, for |x| < 65504)
+ * into fp32 accumulators; each 128 x 128 block scale multiplies its fp32
+ * partial sum.  silu(g) * u is formed in fp32 and stored as f16 (h), each
+ * weighted expert row is stored as f16, the k rows are summed in fp32 in
+ * ascending slot order and the result is rounded once to bf16 (or kept in
+ * fp32 when out_is_fp32 is set).
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer where one is required, negative size, bad alignment */
+    MOE_ERR_UNSUPPORTED = 2,   /* dims outside the limits above */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_size */
+    MOE_ERR_ROUTING = 4,       /* (device) expert id outside [0, E), or a duplicate id when validating */
+    MOE_ERR_TIMEOUT = 5,       /* (device) a pipeline wait exceeded its bound; outputs are unspecified */
+    MOE_ERR_RANGE = 6,         /* (device) an intermediate exceeded the f16 range; outputs hold inf */
+    MOE_ERR_CUDA = 7           /* a CUDA runtime call or launch failed */
+} moe_status;
+
+/* Problem dimensions: d = model width, d_ff = routed expert width,
+ * num_experts = E, top_k = k. */
+typedef struct {
+    int32_t d;
+    int32_t d_ff;
+    int32_t num_experts;
+    int32_t top_k;
+} moe_dims;
+
+/* One bank of FP8 SwiGLU experts (device pointers).
+ *   w_gate, w_up : [E, d_ff, d] e4m3 codes;  s_gate, s_up : [E, d_ff/128, d/128] fp32
+ *   w_down       : [E, d, d_ff] e4m3 codes;  s_down       : [E, d/128, d_ff/128] fp32
+ * Element (r, c) of a matrix dequantises to e4m3(code[r][c]) * s[r/128][c/128].
+ * For the shared expert E = 1 and d_ff is the d_ff_shared argument. */
+typedef struct {
+    const uint8_t *w_gate, *w_up, *w_down;
+    const float *s_gate, *s_up, *s_down;
+} moe_weights;
+
+/* Optional per-kernel timing.  The caller creates up to MOE_TRACE_MAX events;
+ * a call that receives a trace records events[0] before its first kernel and
+ * events[i + 1] after its i-th kernel on `stream`, sets labels[i] to a static
+ * name for that kernel and n_recorded to the number of events recorded.  Pass
+ * NULL to record nothing. */
+#define MOE_TRACE_MAX 16
+typedef struct {
+    cudaEvent_t events[MOE_TRACE_MAX];
+    int32_t n_events;                   /* in: events usable */
+    int32_t n_recorded;                 /* out */
+    const char *labels[MOE_TRACE_MAX];  /* out */
+} moe_trace;
+
+/* Bytes of workspace that every call below needs for n tokens (d_ff_shared =
+ * width of the shared expert, 0 = none).  Returns 0 for unsupported dims. */
+size_t moe_workspace_size(const moe_dims *dims, int64_t n_tokens, int32_t d_ff_shared);
+
+/* Routing plan ("Mixture of experts" page, moe_infer: the per-expert counts
+ * and the sort of the flattened ids by expert).
+ *   topk_ids          [n, k] int32 in
+ *   tokens_per_expert [E]    int32 out: entries with id e
+ *   expert_offsets    [E+1]  int32 out: exclusive prefix sum; offsets[E] = valid entries
+ *   sorted_pos        [n*k]  int32 out: flat index t*k+j of the i-th entry in
+ *                            (expert id, flat index) order - a stable sort; -1 past offsets[E]
+ *   inv_pos           [n*k]  int32 out (may be NULL): inv_pos[sorted_pos[i]] = i; -1 for bad ids
+ *   validate          nonzero: also flag a token that names one expert twice
+ * Bad ids are counted nowhere and raise MOE_ERR_ROUTING on the device. */
+moe_status moe_permute(const moe_dims *dims, int64_t n_tokens, const int32_t *topk_ids,
+                       int32_t *tokens_per_expert, int32_t *expert_offsets, int32_t *sorted_pos,
+                       int32_t *inv_pos, int32_t validate, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Expert pass ("Mixture of experts" page, moe_infer: gather the sorted token
+ * rows, run each expert on its slice, write each output row back to its
+ * position; "SwiGLU output" / "Element-wise product" pages for the expert).
+ *   x               [n, d] bf16 in
+ *   topk_weight     [n, k] fp32 in
+ *   expert_offsets, sorted_pos: as produced by moe_permute for the same topk_ids
+ *   weights         routed bank (struct on the host, tensors on the device)
+ *   rows            [n, k, d] f16 out: rows[t][j] = topk_weight[t][j] * expert_{ids[t][j]}(x[t])
+ * Rows of entries with bad ids are left unwritten. */
+moe_status moe_experts_forward(const moe_dims *dims, int64_t n_tokens, const void *x, const float *topk_weight,
+                               const int32_t *expert_offsets, const int32_t *sorted_pos,
+                               const moe_weights *weights, void *rows, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/* Combine ("Mixture of experts" page, moe_infer: weighted sum over the k
+ * rows; forward: + shared expert; decoder block: + residual).
+ *   out[t] = ((sum_{j=0..k-1} rows[t][j]) + shared[t]) + residual[t]
+ * summed in fp32, j ascending.
+ *   rows      [n, k, d] f16 in
+ *   shared    [n, d] f16 in, or NULL
+ *   residual  [n, d] bf16 in, or NULL
+ *   out       [n, d] bf16, or fp32 when out_is_fp32 != 0 */
+moe_status moe_combine(const moe_dims *dims, int64_t n_tokens, const void *rows, const void *shared,
+                       const void *residual, void *out, int32_t out_is_fp32, cudaStream_t stream);
+
+/* The whole routed-expert forward ("Mixture of experts" page, moe_infer):
+ * moe_permute + moe_experts_forward + moe_combine with every intermediate in
+ * the workspace.  out [n, d] bf16 (fp32 when out_is_fp32).  trace may be NULL. */
+moe_status moe_infer(const moe_dims *dims, int64_t n_tokens, const void *x, const int32_t *topk_ids,
+                     const float *topk_weight, const moe_weights *weights, void *out, int32_t out_is_fp32,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream, moe_trace *trace);
+
+/* The MoE half of a decoder block ("Input features" page, decoder block and
+ * RMSNorm; "Mixture of experts" page, forward):
+ *   xn  = RMSNorm(hidden; gain, eps)                (fp32 arithmetic)
+ *   out = hidden + ( sum_j topk_weight[t][j] * E_{ids[t][j]}(xn) + S(xn) )
+ *   hidden [n, d] bf16, gain [d] bf16, routed bank, shared bank (E = 1,
+ *   width d_ff_shared) or NULL with d_ff_shared = 0.  out as in moe_infer. */
+moe_status moe_layer_forward(const moe_dims *dims, int64_t n_tokens, const void *hidden, const void *gain,
+                             float eps, const int32_t *topk_ids, const float *topk_weight,
+                             const moe_weights *routed, const moe_weights *shared, int32_t d_ff_shared,
+                             void *out, int32_t out_is_fp32, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream, moe_trace *trace);
+
+/* Synchronises `stream`, returns the first device-detected error recorded in
+ * `workspace` since the last call (MOE_OK if none) and clears it. */
+moe_status moe_get_error(void *workspace, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

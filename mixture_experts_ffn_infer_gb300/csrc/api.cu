@@ -1,0 +1,416 @@
+// C ABI of the routed-expert forward: argument checks, workspace layout,
+// tensor-map encoding and the launch sequence of each entry point.  All
+// launches go to the caller's stream; nothing here synchronises except
+// moe_get_error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "moe_ffn.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// ---------------------------------------------------------------- workspace
+struct Layout {
+  size_t err = 0, n_tiles = 64, tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
+  size_t xs = 0, h = 0, xs_sh = 0, h_sh = 0, sh_out = 0, rows = 0, total = 0;
+};
+
+size_t align_up(size_t v) { return (v + 1023) & ~size_t(1023); }
+
+bool dims_ok(const moe_dims* d) {
+  return d && d->d > 0 && d->d_ff > 0 && d->d % 128 == 0 && d->d_ff % 128 == 0 && d->num_experts >= 1 &&
+         d->num_experts <= kMaxExperts && d->top_k >= 1 && d->top_k <= kMaxTopK;
+}
+
+bool make_layout(const moe_dims* d, int64_t n, int32_t dff_sh, Layout* L) {
+  if (!dims_ok(d) || n < 0 || dff_sh < 0 || dff_sh % 128 != 0) return false;
+  const int64_t R = n * d->top_k;
+  if (R >= (int64_t(1) << 31)) return false;
+  const int64_t max_tiles = R / kNTok + d->num_experts + 1;
+  const int64_t max_tiles_sh = n / kNTok + 2;
+  size_t off = 256;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  L->tiles = take(sizeof(TileDesc) * max_tiles);
+  L->tiles_sh = take(sizeof(TileDesc) * max_tiles_sh);
+  L->counts = take(4 * size_t(d->num_experts));
+  L->offsets = take(4 * size_t(d->num_experts + 1));
+  L->sorted_pos = take(4 * size_t(R));
+  L->inv_pos = take(4 * size_t(R));
+  L->xs = take(2 * size_t(R) * d->d);
+  L->h = take(2 * size_t(R) * d->d_ff);
+  L->rows = take(2 * size_t(R) * d->d);
+  if (dff_sh > 0) {
+    L->xs_sh = take(2 * size_t(n) * d->d);
+    L->h_sh = take(2 * size_t(n) * dff_sh);
+    L->sh_out = take(2 * size_t(n) * d->d);
+  }
+  L->total = off;
+  return true;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static std::once_flag once;
+  static EncodeFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// [E][rows][K] e4m3, box 128 (K) x 128 (rows) x 1, 128-byte swizzle.
+bool map_weights(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t E) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {K, rows, E};
+  const cuuint64_t strides[2] = {K, K * rows};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows][K] f16, box 64 (K) x kNTok (rows), 128-byte swizzle; rows past the end read as zero.
+bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNTok)};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool weights_ok(const moe_weights* w) {
+  return w && w->w_gate && w->w_up && w->w_down && w->s_gate && w->s_up && w->s_down && aligned(w->w_gate, 16) &&
+         aligned(w->w_up, 16) && aligned(w->w_down, 16);
+}
+
+struct Tracer {
+  moe_trace* t;
+  cudaStream_t s;
+  void begin() {
+    if (!t) return;
+    t->n_recorded = 0;
+    if (t->n_events > 0 && cudaEventRecord(t->events[0], s) == cudaSuccess) t->n_recorded = 1;
+  }
+  void after(const char* label) {
+    if (!t || t->n_recorded < 1) return;
+    const int i = t->n_recorded;
+    if (i >= t->n_events || i >= MOE_TRACE_MAX) return;
+    t->labels[i - 1] = label;
+    if (cudaEventRecord(t->events[i], s) == cudaSuccess) t->n_recorded = i + 1;
+  }
+};
+
+#define MOE_CHECK_CUDA(expr)                    \
+  do {                                          \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+// The expert pass on an already-sorted routing plan: gather, gate/up, down.
+// `gather` selects the bf16 -> f16 row gather (moe_experts_forward / moe_infer);
+// the fused layer writes the sorted rows itself (RMSNorm scatter).
+moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float* topk_weight,
+                        const int32_t* offsets, const int32_t* sorted_pos, const moe_weights* w, void* rows,
+                        void* ws, const Layout& L, bool gather, cudaStream_t s, Tracer& tr) {
+  const int32_t R = static_cast<int32_t>(n * d->top_k);
+  uint16_t* xs = at<uint16_t>(ws, L.xs);
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  TileDesc* tiles = at<TileDesc>(ws, L.tiles);
+  int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  if (gather) {
+    MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs, s));
+    tr.after("gather_rows");
+  }
+  MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, kNTok, tiles, n_tiles, s));
+  tr.after("build_tiles");
+
+  CUtensorMap m_g, m_u, m_d, m_x, m_h;
+  if (!map_weights(&m_g, w->w_gate, d->d, d->d_ff, d->num_experts) ||
+      !map_weights(&m_u, w->w_up, d->d, d->d_ff, d->num_experts) ||
+      !map_weights(&m_d, w->w_down, d->d_ff, d->d, d->num_experts) || !map_act(&m_x, xs, d->d, R) ||
+      !map_act(&m_h, h, d->d_ff, R))
+    return MOE_ERR_CUDA;
+  GemmLaunch g{};
+  g.w0 = &m_g;
+  g.w1 = &m_u;
+  g.act = &m_x;
+  g.s0 = w->s_gate;
+  g.s1 = w->s_up;
+  g.tiles = tiles;
+  g.n_tiles = n_tiles;
+  g.n_nb = d->d_ff / 128;
+  g.num_kb = d->d / 128;
+  g.out = h;
+  g.err = err;
+  g.num_sms = num_sms();
+  if (g.num_sms <= 0) return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gateup(g, s));
+  tr.after("gateup_swiglu");
+
+  GemmLaunch q = g;
+  q.w0 = &m_d;
+  q.w1 = &m_d;
+  q.act = &m_h;
+  q.s0 = w->s_down;
+  q.s1 = w->s_down;
+  q.n_nb = d->d / 128;
+  q.num_kb = d->d_ff / 128;
+  q.out = rows;
+  q.sorted_pos = sorted_pos;
+  q.topk_weight = topk_weight;
+  MOE_CHECK_CUDA(launch_down(q, s));
+  tr.after("down_scatter");
+  return MOE_OK;
+}
+
+// Shared expert on all n rows of xs_sh (identity order, weight 1) -> sh_out.
+moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32_t dff_sh, void* ws,
+                       const Layout& L, cudaStream_t s, Tracer& tr) {
+  uint16_t* xs = at<uint16_t>(ws, L.xs_sh);
+  uint16_t* h = at<uint16_t>(ws, L.h_sh);
+  TileDesc* tiles = at<TileDesc>(ws, L.tiles_sh);
+  int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
+  MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), kNTok, tiles, n_tiles, s));
+  tr.after("shared_tiles");
+  CUtensorMap m_g, m_u, m_d, m_x, m_h;
+  if (!map_weights(&m_g, w->w_gate, d->d, dff_sh, 1) || !map_weights(&m_u, w->w_up, d->d, dff_sh, 1) ||
+      !map_weights(&m_d, w->w_down, dff_sh, d->d, 1) || !map_act(&m_x, xs, d->d, n) ||
+      !map_act(&m_h, h, dff_sh, n))
+    return MOE_ERR_CUDA;
+  GemmLaunch g{};
+  g.w0 = &m_g;
+  g.w1 = &m_u;
+  g.act = &m_x;
+  g.s0 = w->s_gate;
+  g.s1 = w->s_up;
+  g.tiles = tiles;
+  g.n_tiles = n_tiles;
+  g.n_nb = dff_sh / 128;
+  g.num_kb = d->d / 128;
+  g.out = h;
+  g.err = at<uint32_t>(ws, L.err);
+  g.num_sms = num_sms();
+  if (g.num_sms <= 0) return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gateup(g, s));
+  tr.after("shared_gateup");
+  GemmLaunch q = g;
+  q.w0 = &m_d;
+  q.w1 = &m_d;
+  q.act = &m_h;
+  q.s0 = w->s_down;
+  q.s1 = w->s_down;
+  q.n_nb = d->d / 128;
+  q.num_kb = dff_sh / 128;
+  q.out = at<uint16_t>(ws, L.sh_out);
+  MOE_CHECK_CUDA(launch_down(q, s));
+  tr.after("shared_down");
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_ROUTING: return "MOE_ERR_ROUTING";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_workspace_size(const moe_dims* dims, int64_t n_tokens, int32_t d_ff_shared) {
+  Layout L;
+  if (!make_layout(dims, n_tokens, d_ff_shared, &L)) return 0;
+  return L.total;
+}
+
+moe_status moe_permute(const moe_dims* dims, int64_t n, const int32_t* topk_ids, int32_t* tokens_per_expert,
+                       int32_t* expert_offsets, int32_t* sorted_pos, int32_t* inv_pos, int32_t validate,
+                       void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  if (!tokens_per_expert || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!topk_ids || !sorted_pos)) return MOE_ERR_INVALID_ARG;
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  if (launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, tokens_per_expert,
+                           expert_offsets, sorted_pos, inv_pos, validate, err, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_experts_forward(const moe_dims* dims, int64_t n, const void* x, const float* topk_weight,
+                               const int32_t* expert_offsets, const int32_t* sorted_pos, const moe_weights* w,
+                               void* rows, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (n == 0) return MOE_OK;
+  if (!x || !topk_weight || !expert_offsets || !sorted_pos || !rows || !weights_ok(w) || !aligned(x, 16) ||
+      !aligned(rows, 16))
+    return MOE_ERR_INVALID_ARG;
+  Tracer tr{nullptr, s};
+  return experts_pass(dims, n, x, topk_weight, expert_offsets, sorted_pos, w, rows, ws, L, true, s, tr);
+}
+
+moe_status moe_combine(const moe_dims* dims, int64_t n, const void* rows, const void* shared, const void* residual,
+                       void* out, int32_t out_is_fp32, cudaStream_t s) {
+  if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
+  if (!dims_ok(dims)) return MOE_ERR_UNSUPPORTED;
+  if (n == 0) return MOE_OK;
+  if (!rows || !out || !aligned(rows, 16) || !aligned(out, 16) || (shared && !aligned(shared, 16)) ||
+      (residual && !aligned(residual, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if (launch_combine(static_cast<const uint16_t*>(rows), static_cast<const uint16_t*>(shared),
+                     static_cast<const uint16_t*>(residual), static_cast<int32_t>(n), dims->top_k, dims->d, out,
+                     out_is_fp32, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_infer(const moe_dims* dims, int64_t n, const void* x, const int32_t* topk_ids,
+                     const float* topk_weight, const moe_weights* w, void* out, int32_t out_is_fp32, void* ws,
+                     size_t ws_bytes, cudaStream_t s, moe_trace* trace) {
+  if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (n == 0) return MOE_OK;
+  if (!x || !topk_ids || !topk_weight || !out || !weights_ok(w) || !aligned(x, 16) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  Tracer tr{trace, s};
+  tr.begin();
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* sp = at<int32_t>(ws, L.sorted_pos);
+  int32_t* ip = at<int32_t>(ws, L.inv_pos);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
+                                      offsets, sp, ip, 0, err, s));
+  tr.after("route_permute");
+  void* rows = at<void>(ws, L.rows);
+  moe_status st = experts_pass(dims, n, x, topk_weight, offsets, sp, w, rows, ws, L, true, s, tr);
+  if (st != MOE_OK) return st;
+  MOE_CHECK_CUDA(launch_combine(static_cast<const uint16_t*>(rows), nullptr, nullptr, static_cast<int32_t>(n),
+                                dims->top_k, dims->d, out, out_is_fp32, s));
+  tr.after("combine");
+  return MOE_OK;
+}
+
+moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden, const void* gain, float eps,
+                             const int32_t* topk_ids, const float* topk_weight, const moe_weights* routed,
+                             const moe_weights* shared, int32_t dff_sh, void* out, int32_t out_is_fp32, void* ws,
+                             size_t ws_bytes, cudaStream_t s, moe_trace* trace) {
+  if (!dims || n < 0 || dff_sh < 0) return MOE_ERR_INVALID_ARG;
+  if ((shared == nullptr) != (dff_sh == 0)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(dims, n, dff_sh, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (n == 0) return MOE_OK;
+  if (!hidden || !gain || !topk_ids || !topk_weight || !out || !weights_ok(routed) ||
+      (shared && !weights_ok(shared)) || !aligned(hidden, 16) || !aligned(gain, 16) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  Tracer tr{trace, s};
+  tr.begin();
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* sp = at<int32_t>(ws, L.sorted_pos);
+  int32_t* ip = at<int32_t>(ws, L.inv_pos);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
+                                      offsets, sp, ip, 0, err, s));
+  tr.after("route_permute");
+  MOE_CHECK_CUDA(launch_rmsnorm_scatter(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain),
+                                        eps, static_cast<int32_t>(n), dims->d, dims->top_k, ip,
+                                        at<uint16_t>(ws, L.xs), shared ? at<uint16_t>(ws, L.xs_sh) : nullptr, s));
+  tr.after("rmsnorm_scatter");
+  void* rows = at<void>(ws, L.rows);
+  moe_status st = experts_pass(dims, n, nullptr, topk_weight, offsets, sp, routed, rows, ws, L, false, s, tr);
+  if (st != MOE_OK) return st;
+  if (shared) {
+    st = shared_pass(dims, n, shared, dff_sh, ws, L, s, tr);
+    if (st != MOE_OK) return st;
+  }
+  MOE_CHECK_CUDA(launch_combine(static_cast<const uint16_t*>(rows),
+                                shared ? at<uint16_t>(ws, L.sh_out) : nullptr, static_cast<const uint16_t*>(hidden),
+                                static_cast<int32_t>(n), dims->top_k, dims->d, out, out_is_fp32, s));
+  tr.after("combine");
+  return MOE_OK;
+}
+
+moe_status moe_get_error(void* ws, cudaStream_t s) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&word, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word == 0) return MOE_OK;
+  if (cudaMemset(ws, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (word & DEV_ERR_ROUTING) return MOE_ERR_ROUTING;
+  return MOE_ERR_RANGE;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Shared definitions of the CUDA library: device error bits, the bounded
+// mbarrier wait, tile descriptors and the launchers each .cu file exports.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace moe {
+
+// Bits of the device error word (first 4 bytes of the workspace).
+enum : uint32_t {
+  DEV_ERR_ROUTING = 1u << 0,
+  DEV_ERR_TIMEOUT = 1u << 1,
+  DEV_ERR_RANGE = 1u << 2,
+};
+
+// A pipeline wait gives up after this many SM clocks (about one second at
+// the GB300's maximum clock); it then flags DEV_ERR_TIMEOUT and the kernel
+// winds down instead of hanging the GPU.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// Waits until phase `parity` of the mbarrier has completed.  Returns false
+// (and stops waiting) when another role of the CTA has aborted or when the
+// bound is exceeded, in which case it raises the abort flag itself.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1u;
+      atomicOr(err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// One GEMM tile of the grouped GEMMs: `n_valid` consecutive rows of the
+// sorted activation matrix starting at `row_start`, all routed to `expert`.
+struct TileDesc {
+  int32_t expert;
+  int32_t row_start;
+  int32_t n_valid;
+  int32_t pad;
+};
+
+// Token tile width of the grouped GEMMs (MMA N).
+constexpr int kNTok = 16;
+
+// ---------------------------------------------------------------- launchers
+// routing.cu
+cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32_t E, int32_t* counts,
+                                 int32_t* offsets, int32_t* sorted_pos, int32_t* inv_pos, int32_t validate,
+                                 uint32_t* err, cudaStream_t s);
+cudaError_t launch_build_tiles(const int32_t* offsets, int32_t E, int32_t ntok, TileDesc* tiles,
+                               int32_t* n_tiles, cudaStream_t s);
+cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles, cudaStream_t s);
+
+// elementwise.cu
+cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k,
+                               int32_t d, uint16_t* xs_f16, cudaStream_t s);
+cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_bf16, float eps, int32_t n,
+                                   int32_t d, int32_t k, const int32_t* inv_pos, uint16_t* xs_f16,
+                                   uint16_t* xs_shared_f16, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* rows_f16, const uint16_t* shared_f16, const uint16_t* resid_bf16,
+                           int32_t n, int32_t k, int32_t d, void* out, int32_t out_fp32, cudaStream_t s);
+
+// moe_gemm.cu
+struct GemmLaunch {
+  // weights: 3-D maps over [E][rows][K] e4m3, box 128 x 128 x 1, 128-byte swizzle
+  const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
+  const CUtensorMap* w1;        // up (gate/up pass only)
+  const CUtensorMap* act;       // 2-D map over the sorted activations [rows][K] f16, box 64 x kNTok
+  const float* s0;              // scales [E][n_nb][num_kb]
+  const float* s1;
+  const TileDesc* tiles;
+  const int32_t* n_tiles;
+  int32_t n_nb;                 // weight-row blocks of 128 (output features / 128)
+  int32_t num_kb;               // K / 128
+  void* out;                    // gate/up: h [rows][n_nb*128] f16; down: rows [.][n_nb*128] f16
+  const int32_t* sorted_pos;    // down: flat position of each sorted row (NULL = identity)
+  const float* topk_weight;     // down: flat router weights (NULL = 1)
+  uint32_t* err;
+  int num_sms;
+};
+cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s);
+cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s);
+
+}  // namespace moe

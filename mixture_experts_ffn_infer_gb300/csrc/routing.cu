@@ -1,0 +1,189 @@
+// Routing plan of the routed-expert forward ("Mixture of experts" page,
+// moe_infer: per-expert token counts and the sort of the flattened expert ids).
+//
+// route_permute_kernel: one CTA of 1024 threads replaces the page's one-hot
+// scatter + column sum + argsort with a counting sort that is stable by
+// construction.  Each warp owns a contiguous chunk of the flattened ids and
+// walks it 32 entries at a time; __match_any_sync groups the lanes that carry
+// the same expert so one lane updates the warp's private count (no atomics),
+// and the rank of a lane among its peers is a popcount of the lower peers.
+// Pass 1 builds per-warp histograms in shared memory, a block scan turns them
+// into per-(warp, expert) starting positions, pass 2 repeats the walk and
+// writes sorted_pos / inv_pos.  Order = (expert, warp, round, lane) = (expert,
+// flat index): identical to a stable argsort.
+//
+// build_tiles_kernel: cuts every expert's contiguous slice into tiles of at
+// most `ntok` rows for the grouped GEMMs, on the device, so nothing is copied
+// back to the host (the page's loop reads the counts on the host instead).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+// Exclusive scan of one int per thread over the whole CTA; `*total` gets the sum.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int before = warp > 0 ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[kWarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+route_permute_kernel(const int32_t* __restrict__ ids, int32_t n, int32_t k, int32_t E, int32_t* __restrict__ counts,
+                     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pos, int32_t* __restrict__ inv_pos,
+                     int32_t validate, int32_t reset_err, uint32_t* err) {
+  extern __shared__ int32_t smem[];
+  int32_t* wcnt = smem;                  // [kWarps][E]: counts, then running positions
+  int32_t* warp_sums = smem + kWarps * E;  // [32]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = n * k;
+
+  if (reset_err && tid == 0) *err = 0u;  // a new routing plan starts a new error record
+  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+  __syncthreads();
+
+  // Contiguous chunk of the flattened ids per warp, a multiple of 32 entries.
+  const int chunk = (((R + kWarps - 1) / kWarps) + 31) & ~31;
+  const int beg = min(warp * chunk, R), end = min(beg + chunk, R);
+  int32_t* mine = wcnt + warp * E;
+
+  bool bad = false;
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const int e = i < end ? ids[i] : -1;
+    const bool valid = i < end && e >= 0 && e < E;
+    bad |= (i < end) && !valid;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) atomicOr(err, DEV_ERR_ROUTING);
+  if (validate) {
+    for (int t = tid; t < n; t += kThreads) {
+      const int32_t* row = ids + static_cast<int64_t>(t) * k;
+      bool dup = false;
+      for (int a = 1; a < k; ++a)
+        for (int b = 0; b < a; ++b) dup |= row[a] == row[b];
+      if (dup) atomicOr(err, DEV_ERR_ROUTING);
+    }
+  }
+  __syncthreads();
+
+  // counts[e], offsets[e] and the starting position of each (warp, expert).
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+    for (int w = 0; w < kWarps; ++w) c += wcnt[w * E + e];
+    counts[e] = c;
+    local += c;
+  }
+  int total;
+  int run = block_exclusive_scan(local, warp_sums, &total);
+  for (int e = e0; e < e1; ++e) {
+    offsets[e] = run;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const int e = i < end ? ids[i] : -1;
+    const bool valid = i < end && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid) {
+      const int pos = mine[e] + __popc(peers & ((1u << lane) - 1u));
+      sorted_pos[pos] = i;
+      if (inv_pos) inv_pos[i] = pos;
+    } else if (i < end && inv_pos) {
+      inv_pos[i] = -1;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  for (int i = total + tid; i < R; i += kThreads) sorted_pos[i] = -1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+build_tiles_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t ntok, TileDesc* __restrict__ tiles,
+                   int32_t* __restrict__ n_tiles) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += (offsets[e + 1] - offsets[e] + ntok - 1) / ntok;
+  int total;
+  int t = block_exclusive_scan(local, warp_sums, &total);
+  for (int e = e0; e < e1; ++e) {
+    const int beg = offsets[e], end = offsets[e + 1];
+    for (int r = beg; r < end; r += ntok) tiles[t++] = TileDesc{e, r, min(ntok, end - r), 0};
+  }
+  if (tid == 0) *n_tiles = total;
+}
+
+__global__ void identity_tiles_kernel(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles) {
+  const int nt = (rows + ntok - 1) / ntok;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nt; t += gridDim.x * blockDim.x)
+    tiles[t] = TileDesc{0, t * ntok, min(ntok, rows - t * ntok), 0};
+  if (blockIdx.x == 0 && threadIdx.x == 0) *n_tiles = nt;
+}
+
+}  // namespace
+
+cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32_t E, int32_t* counts,
+                                 int32_t* offsets, int32_t* sorted_pos, int32_t* inv_pos, int32_t validate,
+                                 uint32_t* err, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const size_t smem = sizeof(int32_t) * (static_cast<size_t>(kWarps) * E + 32);
+  cudaError_t e = cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  route_permute_kernel<<<1, kThreads, smem, s>>>(ids, n, k, E, counts, offsets, sorted_pos, inv_pos, validate, 1,
+                                                 err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_tiles(const int32_t* offsets, int32_t E, int32_t ntok, TileDesc* tiles, int32_t* n_tiles,
+                               cudaStream_t s) {
+  build_tiles_kernel<<<1, kThreads, 0, s>>>(offsets, E, ntok, tiles, n_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles, cudaStream_t s) {
+  const int nt = (rows + ntok - 1) / ntok;
+  const int blocks = nt > 0 ? min((nt + 255) / 256, 1024) : 1;
+  identity_tiles_kernel<<<blocks, 256, 0, s>>>(rows, ntok, tiles, n_tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -59,18 +59,21 @@ class Workload:
     full_block: bool = False      # RMSNorm + shared expert + residual
     d_ff_shared: int = 0
     seed: int = 0
+    bank_seed: Optional[int] = None   # seed of the expert bank (default: seed)
 
 
 # The five workloads of the routed-expert forward, named by what they are.
 WORKLOADS = {
     "tiny": Workload("tiny", 128, 1024, 256, 16, 4, seed=0),
-    "k2_decode": Workload("k2_decode", 16, 7168, 2048, 384, 8, seed=1),
-    "k2_prefill": Workload("k2_prefill", 4096, 7168, 2048, 384, 8, seed=2),
+    "k2_decode": Workload("k2_decode", 16, 7168, 2048, 384, 8, seed=1, bank_seed=1),
+    "k2_prefill": Workload("k2_prefill", 4096, 7168, 2048, 384, 8, seed=2, bank_seed=1),
     "k2_skewed": Workload("k2_skewed", 8192, 7168, 2048, 384, 8,
-                          routing="zipf", zipf_s=1.2, seed=3),
+                          routing="zipf", zipf_s=1.2, seed=3, bank_seed=1),
     "k2_block": Workload("k2_block", 32768, 7168, 2048, 384, 8,
-                         full_block=True, d_ff_shared=2048, seed=4),
+                         full_block=True, d_ff_shared=2048, seed=4, bank_seed=1),
 }
+# The four K2-sized workloads share one routed bank (bank_seed 1, 16.9 GB of
+# e4m3 codes) so that a process can keep a single copy resident.
 
 
 def quantize_blockwise(w: torch.Tensor):
@@ -166,8 +169,9 @@ class Inputs:
     shared: Optional[ExpertBank] = None      # E = 1 (full block)
 
 
-def make_inputs(wl: Workload, weight_device="cpu", n_tokens: Optional[int] = None) -> Inputs:
-    """Draw one workload.  ``n_tokens`` overrides N (keeps every other draw's recipe)."""
+def make_host_inputs(wl: Workload, n_tokens: Optional[int] = None):
+    """The host-side draws of a workload: (x bf16 [N, d], topk_ids int32 [N, k], topk_weight fp32 [N, k],
+    gain bf16 [d] or None)."""
     n = wl.n_tokens if n_tokens is None else n_tokens
     g = torch.Generator().manual_seed(wl.seed)
     x = torch.randn(n, wl.d, generator=g).to(torch.bfloat16)
@@ -181,11 +185,24 @@ def make_inputs(wl: Workload, weight_device="cpu", n_tokens: Optional[int] = Non
     gain = None
     if wl.full_block:
         gain = (1.0 + 0.1 * torch.randn(wl.d, generator=g)).to(torch.bfloat16)
-    bank = expert_bank(wl.num_experts, wl.d, wl.d_ff, wl.seed, weight_device)
+    return x, ids, w, gain
+
+
+def make_inputs(wl: Workload, weight_device="cpu", n_tokens: Optional[int] = None,
+                bank: Optional[ExpertBank] = None) -> Inputs:
+    """Draw one workload.  ``n_tokens`` overrides N (keeps every other draw's recipe); ``bank``
+    reuses an expert bank already drawn for the same ``bank_seed``."""
+    x, ids, w, gain = make_host_inputs(wl, n_tokens)
+    bank = bank if bank is not None else expert_bank(wl.num_experts, wl.d, wl.d_ff, bank_seed_of(wl),
+                                                     weight_device)
     shared = None
     if wl.full_block and wl.d_ff_shared:
         shared = expert_bank(1, wl.d, wl.d_ff_shared, wl.seed + 1_000_003, weight_device)
     return Inputs(wl, x, ids, w, bank, gain, 1e-6, shared)
+
+
+def bank_seed_of(wl: Workload) -> int:
+    return wl.seed if wl.bank_seed is None else wl.bank_seed
 
 
 def bank_bytes(d: int, d_ff: int) -> int:
@@ -201,6 +218,7 @@ def touched_experts(topk_ids: torch.Tensor) -> int:
     return int(torch.unique(topk_ids).numel())
 
 
-__all__ = ["Workload", "WORKLOADS", "ExpertBank", "Inputs", "make_inputs", "expert_bank",
+__all__ = ["Workload", "WORKLOADS", "ExpertBank", "Inputs", "make_inputs", "make_host_inputs", "expert_bank",
+           "bank_seed_of",
            "quantize_blockwise", "routing_uniform", "routing_zipf", "routing_subset",
            "router_weights", "bank_bytes", "touched_experts", "ceil_div"]

@@ -241,3 +241,36 @@ def moe_infer_sorted(x, topk_ids, topk_weight, bank):
     y = np.empty((n, d), np.float64)
     lib().oracle_moe_infer_sorted(n, d, dff, k, E, _ptr(xb), _ptr(ids), _ptr(w), *b.args(), _ptr(y))
     return y
+
+
+# --------------------------------------------------------------------------- acceptance criterion
+
+MAX_REL_RMS = 1e-2       # max |y - y_ref| <= 1e-2 * rms(y_ref) (+ half a bf16 ulp when the output is bf16)
+MEAN_REL = 2e-3          # mean |y - y_ref| / mean |y_ref| <= 2e-3
+BF16_HALF_ULP_REL = 2.0 ** -8
+
+
+def parity_report(y, y_ref, bf16_output: bool = True) -> dict:
+    """Compare a library output with the oracle (fp64) under the stated tolerance.
+
+    Per element: |y - y_ref| <= 1e-2 * rms(y_ref) + (2^-8 * |y_ref| if the output is bf16),
+    the second term being the largest rounding error of a bf16 result (half an ulp).
+    Overall: mean |y - y_ref| / mean |y_ref| <= 2e-3."""
+    import torch
+    y = y.detach().to("cpu", torch.float64).numpy() if isinstance(y, torch.Tensor) else np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    err = np.abs(y - y_ref)
+    rms = float(np.sqrt(np.mean(y_ref ** 2)))
+    bound = MAX_REL_RMS * rms + (BF16_HALF_ULP_REL * np.abs(y_ref) if bf16_output else 0.0)
+    excess = float(np.max(err - bound)) if err.size else 0.0
+    mean_rel = float(err.mean() / max(np.abs(y_ref).mean(), 1e-300)) if err.size else 0.0
+    finite = bool(np.isfinite(y).all())
+    return {
+        "ok": finite and excess <= 0.0 and mean_rel <= MEAN_REL,
+        "finite": finite,
+        "max_err_over_rms": float(err.max() / rms) if err.size and rms > 0 else 0.0,
+        "max_excess_over_bound": excess,
+        "mean_rel": mean_rel,
+        "rms_ref": rms,
+        "n": int(err.size),
+    }

@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+entry point that include/moe_ffn.h declares, sizes workspaces and rejects bad
+arguments before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_ffn_infer_gb300 as mx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"^[A-Za-z_][\w \t\*]*?\b(moe_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_ffn_infer_gb300 import build
+    build.build()
+    return mx.load_library()
+
+
+def test_header_declares_the_boundary():
+    assert set(_declared()) >= {"moe_workspace_size", "moe_permute", "moe_experts_forward", "moe_combine",
+                                "moe_infer", "moe_layer_forward", "moe_get_error", "moe_status_string"}
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) == set(mx.exported_symbols())
+
+
+def test_status_strings(lib):
+    for code, name in mx.STATUS.items():
+        assert mx.moe_status_string(code) == name
+
+
+def test_workspace_size_rules(lib):
+    dm = mx.dims(7168, 2048, 384, 8)
+    a = mx.moe_workspace_size(dm, 16)
+    b = mx.moe_workspace_size(dm, 4096)
+    c = mx.moe_workspace_size(dm, 4096, 2048)
+    assert 0 < a < b < c
+    # the big buffers dominate: sorted f16 rows, h and the weighted rows
+    R = 4096 * 8
+    assert b >= 2 * R * 7168 * 2 + 2 * R * 2048
+    assert mx.moe_workspace_size(mx.dims(7168 + 64, 2048, 384, 8), 16) == 0      # d not a multiple of 128
+    assert mx.moe_workspace_size(mx.dims(7168, 2048, 2000, 8), 16) == 0          # too many experts
+    assert mx.moe_workspace_size(mx.dims(7168, 2048, 384, 33), 16) == 0          # k too large
+    assert mx.moe_workspace_size(mx.dims(7168, 2048, 384, 8), 1 << 29) == 0     # n*k >= 2^31
+    assert mx.moe_workspace_size(dm, 16, 100) == 0                              # shared width not x128
+
+
+def test_host_argument_errors_return_codes_without_a_device(lib):
+    dm = mx.dims(1024, 256, 16, 4)
+    w = mx.moe_weights()
+    L = lib
+    # n = 0 is a no-op (needs a workspace pointer only for size checks)
+    buf = (ctypes.c_uint8 * 512)()
+    addr = (ctypes.addressof(buf) + 255) & ~255
+    assert L.moe_combine(ctypes.byref(dm), 0, None, None, None, None, 0, None) == 0
+    # missing workspace
+    assert L.moe_infer(ctypes.byref(dm), 8, None, None, None, ctypes.byref(w), None, 0, None, 0, None, None) == 3
+    # workspace too small
+    assert L.moe_infer(ctypes.byref(dm), 8, None, None, None, ctypes.byref(w), None, 0, ctypes.c_void_p(addr), 256,
+                       None, None) == 3
+    # unsupported dims
+    bad = mx.dims(1000, 256, 16, 4)
+    assert L.moe_infer(ctypes.byref(bad), 8, None, None, None, ctypes.byref(w), None, 0, ctypes.c_void_p(addr),
+                       1 << 30, None, None) == 2
+    # negative n
+    assert L.moe_combine(ctypes.byref(dm), -1, None, None, None, None, 0, None) == 1
+    # null pointers with a large enough (claimed) workspace
+    assert L.moe_infer(ctypes.byref(dm), 8, None, None, None, ctypes.byref(w), None, 0, ctypes.c_void_p(addr),
+                       1 << 30, None, None) == 1
+    # shared expert given without its width
+    assert L.moe_layer_forward(ctypes.byref(dm), 8, None, None, 1e-6, None, None, ctypes.byref(w), ctypes.byref(w),
+                               0, None, 0, ctypes.c_void_p(addr), 1 << 30, None, None) == 1
+    assert L.moe_combine(ctypes.byref(dm), 8, None, None, None, None, 0, None) == 1
+    assert L.moe_get_error(None, None) == 1

@@ -1,0 +1,158 @@
+"""The CUDA path against the CPU oracle on the same seeded inputs.
+
+Tolerance (stated for the routed-expert forward): per element
+|y - y_ref| <= 1e-2 * rms(y_ref) (+ 2^-8 |y_ref|, half a bf16 ulp, for a bf16
+output) and mean |y - y_ref| / mean |y_ref| <= 2e-3.  Small workloads are
+compared element by element over the whole output; K2-sized ones on a seeded
+token sample (uniform tokens plus tokens of the most loaded expert) that the
+oracle computes one by one, at the full size and launch configuration."""
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_infer_gb300 as mx
+import oracle
+from mixture_experts_ffn_infer_gb300 import synthetic as syn
+from tests import gpu_cases as cases
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert_ok(y, ref, bf16=True):
+    rep = oracle.parity_report(y, ref, bf16)
+    assert rep["ok"], rep
+    return rep
+
+
+# ------------------------------------------------------------------ small, whole output
+
+def test_tiny_infer_bf16_and_fp32_outputs():
+    c = cases.workload("tiny")
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
+    y = mx.infer(c.x, c.ids, c.w, c.bank)
+    _assert_ok(y, ref, bf16=True)
+    y32 = mx.infer(c.x, c.ids, c.w, c.bank, out_is_fp32=True)
+    _assert_ok(y32, ref, bf16=False)
+    assert torch.equal(y32.to(torch.bfloat16), y)   # the bf16 output is the fp32 result rounded once
+
+
+@pytest.mark.parametrize("n,d,dff,E,k,seed", [
+    (37, 256, 384, 5, 3, 1),       # ragged token count, d_ff of three 128-blocks
+    (1, 1024, 256, 16, 4, 2),      # one token
+    (200, 512, 128, 64, 6, 3),     # many experts, most with few rows
+    (300, 384, 256, 3, 1, 4),      # k = 1, a hundred rows per expert (several token tiles)
+    (64, 128, 128, 1, 1, 5),       # single expert
+])
+def test_small_shapes_infer(n, d, dff, E, k, seed):
+    wl = syn.Workload("s", n, d, dff, E, k, seed=seed)
+    c = cases.workload(wl)
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
+    _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank), ref)
+    _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank, out_is_fp32=True), ref, bf16=False)
+
+
+def test_experts_forward_rows_and_combine_separately():
+    c = cases.workload("tiny")
+    n, k, d = c.inp.wl.n_tokens, c.inp.wl.top_k, c.inp.wl.d
+    dm = mx.dims(d, c.inp.wl.d_ff, c.inp.wl.num_experts, k)
+    ws = mx.workspace(dm, n)
+    counts, offsets, sp, ip = mx.permute(c.ids, c.inp.wl.num_experts, ws=ws)
+    rows = torch.empty(n, k, d, dtype=torch.float16, device="cuda")
+    mx.moe_experts_forward(dm, n, c.x, c.w, offsets, sp, mx.weights(c.bank), rows, ws)
+    # each row is topk_weight * expert(x) for its own (token, slot)
+    for t, j in [(0, 0), (0, 3), (77, 1), (127, 2)]:
+        e = int(c.inp.topk_ids[t, j])
+        b = c.inp.bank
+        o = oracle.expert_forward(c.inp.x[t:t + 1].double().numpy(), b.w_gate[e], b.s_gate[e], b.w_up[e],
+                                  b.s_up[e], b.w_down[e], b.s_down[e])[0] * float(c.inp.topk_weight[t, j])
+        got = rows[t, j].double().cpu().numpy()
+        rms = np.sqrt(np.mean(o ** 2))
+        assert np.max(np.abs(got - o) - 2.0 ** -10 * np.abs(o)) <= 1e-2 * rms
+    out = torch.empty(n, d, dtype=torch.float32, device="cuda")
+    mx.moe_combine(dm, n, rows, None, None, out, out_is_fp32=True)
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
+    _assert_ok(out, ref, bf16=False)
+    # combine is an ordered fp32 sum of the f16 rows
+    assert torch.equal(out, rows.float().sum(dim=1)) or torch.allclose(out, rows.float().sum(dim=1), rtol=0,
+                                                                        atol=1e-6)
+    assert mx.moe_get_error(ws) == mx.MOE_OK
+
+
+def test_combine_adds_shared_then_residual():
+    n, k, d = 19, 3, 256
+    g = torch.Generator().manual_seed(3)
+    rows = torch.randn(n, k, d, generator=g).half().cuda()
+    shared = torch.randn(n, d, generator=g).half().cuda()
+    resid = torch.randn(n, d, generator=g).bfloat16().cuda()
+    dm = mx.dims(d, 128, 4, k)
+    out = torch.empty(n, d, dtype=torch.float32, device="cuda")
+    mx.moe_combine(dm, n, rows, shared, resid, out, out_is_fp32=True)
+    r = rows.double()
+    ref = ((r[:, 0] + r[:, 1] + r[:, 2]) + shared.double()) + resid.double()
+    assert torch.allclose(out.double(), ref, rtol=1e-6, atol=1e-6)
+    outb = torch.empty(n, d, dtype=torch.bfloat16, device="cuda")
+    mx.moe_combine(dm, n, rows, shared, resid, outb)
+    assert torch.equal(outb, out.to(torch.bfloat16))
+
+
+def test_layer_forward_small_with_shared_expert():
+    wl = syn.Workload("blk", 96, 512, 256, 12, 4, full_block=True, d_ff_shared=384, seed=7)
+    c = cases.workload(wl)
+    ref = oracle.layer_forward(c.inp.x, c.inp.gain, c.inp.eps, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank,
+                               c.inp.shared)
+    y = mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, c.shared)
+    _assert_ok(y, ref)
+    y2 = mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, None)
+    ref2 = oracle.layer_forward(c.inp.x, c.inp.gain, c.inp.eps, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
+    _assert_ok(y2, ref2)
+
+
+def test_deterministic_and_zero_tokens():
+    c = cases.workload("tiny")
+    a = mx.infer(c.x, c.ids, c.w, c.bank)
+    b = mx.infer(c.x, c.ids, c.w, c.bank)
+    assert torch.equal(a, b)
+    empty = mx.infer(c.x[:0], c.ids[:0], c.w[:0], c.bank)
+    assert empty.shape == (0, c.x.shape[1])
+
+
+def test_forced_empty_experts_and_hot_expert():
+    wl = syn.Workload("s", 256, 512, 256, 64, 4, seed=9)
+    g = torch.Generator().manual_seed(2)
+    ids = syn.routing_subset(256, [3, 17, 40, 41, 63], 4, g)
+    c = cases.workload(wl, ids=ids)
+    c.ids = ids.cuda()
+    ref = oracle.moe_infer(c.inp.x, ids, c.inp.topk_weight, c.inp.bank)
+    _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank), ref)
+
+
+# ------------------------------------------------------------------ K2 sizes
+
+def test_k2_decode_whole_output():
+    c = cases.workload("k2_decode")
+    y = mx.infer(c.x, c.ids, c.w, c.bank)
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.bank)
+    _assert_ok(y, ref)
+    y32 = mx.infer(c.x, c.ids, c.w, c.bank, out_is_fp32=True)
+    _assert_ok(y32, ref, bf16=False)
+
+
+@pytest.mark.parametrize("name,n_random,n_hot", [("k2_prefill", 24, 8), ("k2_skewed", 24, 16)])
+def test_k2_large_sampled_tokens(name, n_random, n_hot):
+    c = cases.workload(name)
+    y = mx.infer(c.x, c.ids, c.w, c.bank)
+    tok = cases.sample_tokens(c.inp.topk_ids, n_random, n_hot, seed=1)
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.bank, tokens=tok)
+    _assert_ok(y[tok], ref)
+    assert torch.isfinite(y.float()).all()
+
+
+def test_k2_block_sampled_tokens():
+    c = cases.workload("k2_block")
+    y = mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, c.shared)
+    tok = cases.sample_tokens(c.inp.topk_ids, 16, 8, seed=2)
+    ref = oracle.layer_forward(c.inp.x, c.inp.gain, c.inp.eps, c.inp.topk_ids, c.inp.topk_weight, c.bank,
+                               c.shared, tokens=tok)
+    _assert_ok(y[tok], ref)
+    assert torch.isfinite(y.float()).all()
