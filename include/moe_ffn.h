@@ -78,14 +78,21 @@ typedef struct {
     int32_t top_k;
 } moe_dims;
 
+/* Layout of the e4m3 codes of a bank. */
+#define MOE_LAYOUT_ROW_MAJOR 0  /* [E][rows][cols], as the model stores them */
+#define MOE_LAYOUT_TILED 1      /* moe_pack_weights output: one contiguous 16 KB block per 128 x 128 tile */
+
 /* One bank of FP8 SwiGLU experts (device pointers).
  *   w_gate, w_up : [E, d_ff, d] e4m3 codes;  s_gate, s_up : [E, d_ff/128, d/128] fp32
  *   w_down       : [E, d, d_ff] e4m3 codes;  s_down       : [E, d/128, d_ff/128] fp32
  * Element (r, c) of a matrix dequantises to e4m3(code[r][c]) * s[r/128][c/128].
+ * With layout MOE_LAYOUT_TILED the code arrays hold the same bytes rearranged
+ * by moe_pack_weights (same total size); the scales never change layout.
  * For the shared expert E = 1 and d_ff is the d_ff_shared argument. */
 typedef struct {
     const uint8_t *w_gate, *w_up, *w_down;
     const float *s_gate, *s_up, *s_down;
+    int32_t layout;         /* MOE_LAYOUT_ROW_MAJOR or MOE_LAYOUT_TILED */
 } moe_weights;
 
 /* Optional per-kernel timing.  The caller creates up to MOE_TRACE_MAX events;
@@ -104,6 +111,21 @@ typedef struct {
 /* Bytes of workspace that every call below needs for n tokens (d_ff_shared =
  * width of the shared expert, 0 = none).  Returns 0 for unsupported dims. */
 size_t moe_workspace_size(const moe_dims *dims, int64_t n_tokens, int32_t d_ff_shared);
+
+/* Weight preparation for streaming (no counterpart on the pages: a storage
+ * layout, not arithmetic).  Rearranges the e4m3 codes of a row-major bank
+ * (src->layout must be MOE_LAYOUT_ROW_MAJOR) into MOE_LAYOUT_TILED: for each
+ * matrix, expert e, 128-row block b and 128-column block c, the 16384 codes of
+ * that tile become one contiguous block at offset ((e * R/128 + b) * C/128 + c)
+ * * 16384, row r of the tile at r * 128 with its 16-byte chunk j stored at
+ * chunk position j ^ (r % 8).  A unit of work then streams one contiguous
+ * region instead of 128-byte pieces of 128 rows.
+ *   num_experts, d, d_ff: the bank's sizes (d_ff = d_ff_shared for a shared expert)
+ *   src: row-major codes; dst: caller-allocated code buffers of the same sizes
+ *        (dst->s_* and dst->layout are not read).  src and dst must not overlap.
+ * Asynchronous on `stream`; call once when the weights are loaded. */
+moe_status moe_pack_weights(int32_t num_experts, int32_t d, int32_t d_ff, const moe_weights *src,
+                            const moe_weights *dst, cudaStream_t stream);
 
 /* Routing plan ("Mixture of experts" page, moe_infer: the per-expert counts
  * and the sort of the flattened ids by expert).

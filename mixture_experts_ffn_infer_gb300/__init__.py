@@ -39,9 +39,14 @@ class moe_dims(ctypes.Structure):
                 ("top_k", ctypes.c_int32)]
 
 
+MOE_LAYOUT_ROW_MAJOR = 0
+MOE_LAYOUT_TILED = 1
+
+
 class moe_weights(ctypes.Structure):
     _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
-                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p)]
+                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("layout", ctypes.c_int32)]
 
 
 class moe_trace(ctypes.Structure):
@@ -55,6 +60,8 @@ _lock = threading.Lock()
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_dims), ctypes.c_int64, ctypes.c_int32]),
+    "moe_pack_weights": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(moe_weights),
+                                         ctypes.POINTER(moe_weights), ctypes.c_void_p]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 5
                     + [ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_experts_forward": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 4
@@ -118,9 +125,11 @@ def dims(d: int, d_ff: int, num_experts: int, top_k: int) -> moe_dims:
 
 
 def weights(bank) -> moe_weights:
-    """moe_weights from an object with w_gate/w_up/w_down/s_gate/s_up/s_down device tensors."""
+    """moe_weights from an object with w_gate/w_up/w_down/s_gate/s_up/s_down device tensors
+    (and an optional ``layout`` attribute, default row-major)."""
     return moe_weights(*(bank_t.data_ptr() for bank_t in (bank.w_gate, bank.w_up, bank.w_down, bank.s_gate,
-                                                          bank.s_up, bank.s_down)))
+                                                          bank.s_up, bank.s_down)),
+                       int(getattr(bank, "layout", MOE_LAYOUT_ROW_MAJOR)))
 
 
 # ---------------------------------------------------------------- C entry points (same names)
@@ -131,6 +140,12 @@ def moe_status_string(status: int) -> str:
 
 def moe_workspace_size(dm: moe_dims, n_tokens: int, d_ff_shared: int = 0) -> int:
     return load_library().moe_workspace_size(ctypes.byref(dm), n_tokens, d_ff_shared)
+
+
+def moe_pack_weights(num_experts, d, d_ff, src: moe_weights, dst: moe_weights, stream=None):
+    st = load_library().moe_pack_weights(num_experts, d, d_ff, ctypes.byref(src), ctypes.byref(dst),
+                                         _stream(stream))
+    _check(st, "moe_pack_weights")
 
 
 def moe_permute(dm, n_tokens, topk_ids, tokens_per_expert, expert_offsets, sorted_pos, inv_pos, ws,
@@ -181,6 +196,26 @@ def moe_get_error(ws, stream=None) -> int:
 
 
 # ---------------------------------------------------------------- allocating conveniences
+
+class TiledBank:
+    """A bank whose e4m3 codes are in the tiled streaming layout (tensors keep their shapes)."""
+
+    layout = MOE_LAYOUT_TILED
+
+    def __init__(self, w_gate, w_up, w_down, s_gate, s_up, s_down):
+        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+        self.s_gate, self.s_up, self.s_down = s_gate, s_up, s_down
+
+
+def pack_bank(bank, stream=None) -> TiledBank:
+    """Tiled copy of a row-major bank's codes (scales shared with the source)."""
+    import torch
+    E, d_ff, d = bank.w_gate.shape
+    out = TiledBank(torch.empty_like(bank.w_gate), torch.empty_like(bank.w_up), torch.empty_like(bank.w_down),
+                    bank.s_gate, bank.s_up, bank.s_down)
+    moe_pack_weights(E, d, d_ff, weights(bank), weights(out), stream)
+    return out
+
 
 def workspace(dm: moe_dims, n_tokens: int, d_ff_shared: int = 0, device="cuda"):
     import torch

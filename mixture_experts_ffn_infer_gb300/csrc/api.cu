@@ -19,9 +19,12 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 
 // ---------------------------------------------------------------- workspace
+// Sorted activations and h are kept in the split format (split3.cuh): e4m3
+// codes [3 rows][width] plus one fp32 exponent factor per (128 columns, row).
 struct Layout {
   size_t err = 0, n_tiles = 64, tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
-  size_t xs = 0, h = 0, xs_sh = 0, h_sh = 0, sh_out = 0, rows = 0, total = 0;
+  size_t xs = 0, xs_inv = 0, h = 0, h_inv = 0, xs_sh = 0, xs_sh_inv = 0, h_sh = 0, h_sh_inv = 0, sh_out = 0;
+  size_t rows = 0, total = 0;
 };
 
 size_t align_up(size_t v) { return (v + 1023) & ~size_t(1023); }
@@ -49,12 +52,16 @@ bool make_layout(const moe_dims* d, int64_t n, int32_t dff_sh, Layout* L) {
   L->offsets = take(4 * size_t(d->num_experts + 1));
   L->sorted_pos = take(4 * size_t(R));
   L->inv_pos = take(4 * size_t(R));
-  L->xs = take(2 * size_t(R) * d->d);
-  L->h = take(2 * size_t(R) * d->d_ff);
+  L->xs = take(3 * size_t(R) * d->d);
+  L->xs_inv = take(4 * size_t(R) * (d->d / 128));
+  L->h = take(3 * size_t(R) * d->d_ff);
+  L->h_inv = take(4 * size_t(R) * (d->d_ff / 128));
   L->rows = take(2 * size_t(R) * d->d);
   if (dff_sh > 0) {
-    L->xs_sh = take(2 * size_t(n) * d->d);
-    L->h_sh = take(2 * size_t(n) * dff_sh);
+    L->xs_sh = take(3 * size_t(n) * d->d);
+    L->xs_sh_inv = take(4 * size_t(n) * (d->d / 128));
+    L->h_sh = take(3 * size_t(n) * dff_sh);
+    L->h_sh_inv = take(4 * size_t(n) * (dff_sh / 128));
     L->sh_out = take(2 * size_t(n) * d->d);
   }
   L->total = off;
@@ -98,15 +105,16 @@ bool map_weights(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][K] f16, box 64 (K) x kNTok (rows), 128-byte swizzle; rows past the end read as zero.
+// Split-format codes of `rows` sorted rows: [3 rows][K] e4m3, box 128 (K) x 3 kNTok
+// (three terms of kNTok rows), 128-byte swizzle; rows past the end read as zero.
 bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
   EncodeFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {K, rows};
-  const cuuint64_t strides[1] = {K * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNTok)};
+  const cuuint64_t dims[2] = {K, 3 * rows};
+  const cuuint64_t strides[1] = {K};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(3 * kNTok)};
   const cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -129,7 +137,16 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool weights_ok(const moe_weights* w) {
   return w && w->w_gate && w->w_up && w->w_down && w->s_gate && w->s_up && w->s_down && aligned(w->w_gate, 16) &&
-         aligned(w->w_up, 16) && aligned(w->w_down, 16);
+         aligned(w->w_up, 16) && aligned(w->w_down, 16) &&
+         (w->layout == MOE_LAYOUT_ROW_MAJOR || w->layout == MOE_LAYOUT_TILED);
+}
+
+// Weight maps of a bank (row-major only; the tiled layout is read with bulk copies).
+bool map_bank(const moe_weights* w, int64_t d, int64_t dff, int64_t E, CUtensorMap* g, CUtensorMap* u,
+              CUtensorMap* dn) {
+  if (w->layout == MOE_LAYOUT_TILED) return true;
+  return map_weights(g, w->w_gate, d, dff, E) && map_weights(u, w->w_up, d, dff, E) &&
+         map_weights(dn, w->w_down, dff, d, E);
 }
 
 struct Tracer {
@@ -161,27 +178,31 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
                         const int32_t* offsets, const int32_t* sorted_pos, const moe_weights* w, void* rows,
                         void* ws, const Layout& L, bool gather, cudaStream_t s, Tracer& tr) {
   const int32_t R = static_cast<int32_t>(n * d->top_k);
-  uint16_t* xs = at<uint16_t>(ws, L.xs);
-  uint16_t* h = at<uint16_t>(ws, L.h);
+  uint8_t* xs = at<uint8_t>(ws, L.xs);
+  float* xs_inv = at<float>(ws, L.xs_inv);
+  uint8_t* h = at<uint8_t>(ws, L.h);
+  float* h_inv = at<float>(ws, L.h_inv);
   TileDesc* tiles = at<TileDesc>(ws, L.tiles);
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (gather) {
-    MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs, s));
+    MOE_CHECK_CUDA(
+        launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs, xs_inv, s));
     tr.after("gather_rows");
   }
   MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, kNTok, tiles, n_tiles, s));
   tr.after("build_tiles");
 
   CUtensorMap m_g, m_u, m_d, m_x, m_h;
-  if (!map_weights(&m_g, w->w_gate, d->d, d->d_ff, d->num_experts) ||
-      !map_weights(&m_u, w->w_up, d->d, d->d_ff, d->num_experts) ||
-      !map_weights(&m_d, w->w_down, d->d_ff, d->d, d->num_experts) || !map_act(&m_x, xs, d->d, R) ||
-      !map_act(&m_h, h, d->d_ff, R))
-    return MOE_ERR_CUDA;
+  if (!map_act(&m_x, xs, d->d, R) || !map_act(&m_h, h, d->d_ff, R)) return MOE_ERR_CUDA;
+  m_g = m_u = m_d = m_x;  // placeholders when the bank is tiled
+  if (!map_bank(w, d->d, d->d_ff, d->num_experts, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
+  const bool tiled = w->layout == MOE_LAYOUT_TILED;
   GemmLaunch g{};
   g.w0 = &m_g;
   g.w1 = &m_u;
+  g.w0_tiled = tiled ? w->w_gate : nullptr;
+  g.w1_tiled = tiled ? w->w_up : nullptr;
   g.act = &m_x;
   g.s0 = w->s_gate;
   g.s1 = w->s_up;
@@ -189,7 +210,10 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
   g.n_tiles = n_tiles;
   g.n_nb = d->d_ff / 128;
   g.num_kb = d->d / 128;
+  g.act_inv = xs_inv;
+  g.act_rows = R;
   g.out = h;
+  g.out_inv = h_inv;
   g.err = err;
   g.num_sms = num_sms();
   if (g.num_sms <= 0) return MOE_ERR_CUDA;
@@ -199,12 +223,15 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
   GemmLaunch q = g;
   q.w0 = &m_d;
   q.w1 = &m_d;
+  q.w0_tiled = q.w1_tiled = tiled ? w->w_down : nullptr;
   q.act = &m_h;
   q.s0 = w->s_down;
   q.s1 = w->s_down;
   q.n_nb = d->d / 128;
   q.num_kb = d->d_ff / 128;
+  q.act_inv = h_inv;
   q.out = rows;
+  q.out_inv = nullptr;
   q.sorted_pos = sorted_pos;
   q.topk_weight = topk_weight;
   MOE_CHECK_CUDA(launch_down(q, s));
@@ -215,20 +242,24 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
 // Shared expert on all n rows of xs_sh (identity order, weight 1) -> sh_out.
 moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32_t dff_sh, void* ws,
                        const Layout& L, cudaStream_t s, Tracer& tr) {
-  uint16_t* xs = at<uint16_t>(ws, L.xs_sh);
-  uint16_t* h = at<uint16_t>(ws, L.h_sh);
+  uint8_t* xs = at<uint8_t>(ws, L.xs_sh);
+  float* xs_inv = at<float>(ws, L.xs_sh_inv);
+  uint8_t* h = at<uint8_t>(ws, L.h_sh);
+  float* h_inv = at<float>(ws, L.h_sh_inv);
   TileDesc* tiles = at<TileDesc>(ws, L.tiles_sh);
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
   MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), kNTok, tiles, n_tiles, s));
   tr.after("shared_tiles");
   CUtensorMap m_g, m_u, m_d, m_x, m_h;
-  if (!map_weights(&m_g, w->w_gate, d->d, dff_sh, 1) || !map_weights(&m_u, w->w_up, d->d, dff_sh, 1) ||
-      !map_weights(&m_d, w->w_down, dff_sh, d->d, 1) || !map_act(&m_x, xs, d->d, n) ||
-      !map_act(&m_h, h, dff_sh, n))
-    return MOE_ERR_CUDA;
+  if (!map_act(&m_x, xs, d->d, n) || !map_act(&m_h, h, dff_sh, n)) return MOE_ERR_CUDA;
+  m_g = m_u = m_d = m_x;
+  if (!map_bank(w, d->d, dff_sh, 1, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
+  const bool tiled = w->layout == MOE_LAYOUT_TILED;
   GemmLaunch g{};
   g.w0 = &m_g;
   g.w1 = &m_u;
+  g.w0_tiled = tiled ? w->w_gate : nullptr;
+  g.w1_tiled = tiled ? w->w_up : nullptr;
   g.act = &m_x;
   g.s0 = w->s_gate;
   g.s1 = w->s_up;
@@ -236,7 +267,10 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
   g.n_tiles = n_tiles;
   g.n_nb = dff_sh / 128;
   g.num_kb = d->d / 128;
+  g.act_inv = xs_inv;
+  g.act_rows = static_cast<int32_t>(n);
   g.out = h;
+  g.out_inv = h_inv;
   g.err = at<uint32_t>(ws, L.err);
   g.num_sms = num_sms();
   if (g.num_sms <= 0) return MOE_ERR_CUDA;
@@ -245,12 +279,15 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
   GemmLaunch q = g;
   q.w0 = &m_d;
   q.w1 = &m_d;
+  q.w0_tiled = q.w1_tiled = tiled ? w->w_down : nullptr;
   q.act = &m_h;
   q.s0 = w->s_down;
   q.s1 = w->s_down;
   q.n_nb = d->d / 128;
   q.num_kb = dff_sh / 128;
+  q.act_inv = h_inv;
   q.out = at<uint16_t>(ws, L.sh_out);
+  q.out_inv = nullptr;
   MOE_CHECK_CUDA(launch_down(q, s));
   tr.after("shared_down");
   return MOE_OK;
@@ -281,6 +318,26 @@ size_t moe_workspace_size(const moe_dims* dims, int64_t n_tokens, int32_t d_ff_s
   Layout L;
   if (!make_layout(dims, n_tokens, d_ff_shared, &L)) return 0;
   return L.total;
+}
+
+moe_status moe_pack_weights(int32_t E, int32_t d, int32_t dff, const moe_weights* src, const moe_weights* dst,
+                            cudaStream_t s) {
+  if (!src || !dst) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || d <= 0 || dff <= 0 || d % 128 != 0 || dff % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (src->layout != MOE_LAYOUT_ROW_MAJOR) return MOE_ERR_INVALID_ARG;
+  const uint8_t* in[3] = {src->w_gate, src->w_up, src->w_down};
+  const uint8_t* out[3] = {dst->w_gate, dst->w_up, dst->w_down};
+  const int32_t rows[3] = {dff, dff, d}, cols[3] = {d, d, dff};
+  const size_t bytes = static_cast<size_t>(E) * d * dff;
+  for (int m = 0; m < 3; ++m) {
+    if (!in[m] || !out[m] || !aligned(in[m], 16) || !aligned(out[m], 16)) return MOE_ERR_INVALID_ARG;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(in[m]), b0 = reinterpret_cast<uintptr_t>(out[m]);
+    if (a0 < b0 + bytes && b0 < a0 + bytes) return MOE_ERR_INVALID_ARG;  // overlapping buffers
+  }
+  for (int m = 0; m < 3; ++m)
+    if (launch_pack_tiles(in[m], const_cast<uint8_t*>(out[m]), E, rows[m], cols[m], s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status moe_permute(const moe_dims* dims, int64_t n, const int32_t* topk_ids, int32_t* tokens_per_expert,
@@ -384,8 +441,9 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
                                       offsets, sp, ip, 0, err, s));
   tr.after("route_permute");
   MOE_CHECK_CUDA(launch_rmsnorm_scatter(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain),
-                                        eps, static_cast<int32_t>(n), dims->d, dims->top_k, ip,
-                                        at<uint16_t>(ws, L.xs), shared ? at<uint16_t>(ws, L.xs_sh) : nullptr, s));
+                                        eps, static_cast<int32_t>(n), dims->d, dims->top_k, ip, at<uint8_t>(ws, L.xs),
+                                        at<float>(ws, L.xs_inv), shared ? at<uint8_t>(ws, L.xs_sh) : nullptr,
+                                        shared ? at<float>(ws, L.xs_sh_inv) : nullptr, s));
   tr.after("rmsnorm_scatter");
   void* rows = at<void>(ws, L.rows);
   moe_status st = experts_pass(dims, n, nullptr, topk_weight, offsets, sp, routed, rows, ws, L, false, s, tr);

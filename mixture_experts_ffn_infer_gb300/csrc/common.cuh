@@ -63,11 +63,14 @@ cudaError_t launch_build_tiles(const int32_t* offsets, int32_t E, int32_t ntok, 
 cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles, cudaStream_t s);
 
 // elementwise.cu
+// Sorted activation rows in the split format: codes [3 R][d] e4m3 + exponents [d/128][R].
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k,
-                               int32_t d, uint16_t* xs_f16, cudaStream_t s);
+                               int32_t d, uint8_t* xs, float* xs_inv, cudaStream_t s);
 cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_bf16, float eps, int32_t n,
-                                   int32_t d, int32_t k, const int32_t* inv_pos, uint16_t* xs_f16,
-                                   uint16_t* xs_shared_f16, cudaStream_t s);
+                                   int32_t d, int32_t k, const int32_t* inv_pos, uint8_t* xs, float* xs_inv,
+                                   uint8_t* xs_shared, float* xs_shared_inv, cudaStream_t s);
+cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_experts, int32_t rows, int32_t cols,
+                              cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* rows_f16, const uint16_t* shared_f16, const uint16_t* resid_bf16,
                            int32_t n, int32_t k, int32_t d, void* out, int32_t out_fp32, cudaStream_t s);
 
@@ -76,14 +79,19 @@ struct GemmLaunch {
   // weights: 3-D maps over [E][rows][K] e4m3, box 128 x 128 x 1, 128-byte swizzle
   const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
   const CUtensorMap* w1;        // up (gate/up pass only)
-  const CUtensorMap* act;       // 2-D map over the sorted activations [rows][K] f16, box 64 x kNTok
+  const CUtensorMap* act;       // 2-D map over the split activations [3 rows][K] e4m3, box 128 x 3 kNTok
+  const uint8_t* w0_tiled;      // tiled layout (moe_pack_weights): used instead of w0 / w1 when non-null
+  const uint8_t* w1_tiled;
   const float* s0;              // scales [E][n_nb][num_kb]
   const float* s1;
   const TileDesc* tiles;
   const int32_t* n_tiles;
   int32_t n_nb;                 // weight-row blocks of 128 (output features / 128)
   int32_t num_kb;               // K / 128
-  void* out;                    // gate/up: h [rows][n_nb*128] f16; down: rows [.][n_nb*128] f16
+  const float* act_inv;         // [num_kb][act_rows] 2^-s of each activation block
+  int32_t act_rows;             // rows of the sorted activation matrix
+  void* out;                    // gate/up: h terms [3 act_rows][n_nb*128] e4m3; down: rows [.][n_nb*128] f16
+  float* out_inv;               // gate/up: [n_nb][act_rows] 2^-s of each h block
   const int32_t* sorted_pos;    // down: flat position of each sorted row (NULL = identity)
   const float* topk_weight;     // down: flat router weights (NULL = 1)
   uint32_t* err;

@@ -1,12 +1,16 @@
 // Bandwidth-bound steps around the grouped GEMMs.
 //
 // gather_rows_kernel    - "Mixture of experts" page, moe_infer: sorted_tokens
-//                         = x[idxs // k]; rows are converted bf16 -> f16 (exact
-//                         for |x| < 65504) for the f16 tensor-core GEMMs.
+//                         = x[idxs // k]; rows are written in the three-term
+//                         e4m3 split format the GEMMs read (split3.cuh).
 // rmsnorm_scatter_kernel- "Input features" page, RMSNorm: fp32 mean of squares,
 //                         rsqrt(mean + eps), times gain; the normalised row is
-//                         written once per routed slot straight to its sorted
-//                         position (inv_pos) and to the shared expert's rows.
+//                         split once and written per routed slot straight to its
+//                         sorted position (inv_pos) and to the shared expert's rows.
+// pack_tiles_kernel     - storage layout only: copies each 128 x 128 tile of
+//                         e4m3 codes into one contiguous 16 KB block, laid out
+//                         exactly as a 128-byte-swizzled TMA box lands in
+//                         shared memory, so the GEMM streams it with one bulk copy.
 // combine_kernel        - "Mixture of experts" page, moe_infer: sum of the
 //                         token's k weighted rows (fp32, ascending slot), plus
 //                         the shared expert ("forward") and the residual
@@ -16,6 +20,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "split3.cuh"
 
 namespace moe {
 namespace {
@@ -35,39 +40,43 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) { return pack_f16x2(bf16_lo(w), bf16_hi(w)); }
+constexpr int kRowThreads = 256;  // eight warps per row, one 128-column block per warp at a time
 
-__global__ void __launch_bounds__(128) gather_rows_kernel(const uint16_t* __restrict__ x,
-                                                          const int32_t* __restrict__ sorted_pos, int32_t k,
-                                                          int32_t d, uint16_t* __restrict__ xs) {
+__global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                                  const int32_t* __restrict__ sorted_pos, int32_t R,
+                                                                  int32_t k, int32_t d, uint8_t* __restrict__ xs,
+                                                                  float* __restrict__ xs_inv) {
   const int64_t i = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = sorted_pos[i];
-  uint4* dst = reinterpret_cast<uint4*>(xs + i * d);
-  const int nv = d / 8;
-  if (p < 0) {
-    for (int c = threadIdx.x; c < nv; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(p / k) * d);
-  for (int c = threadIdx.x; c < nv; c += blockDim.x) {
-    const uint4 v = src[c];
-    dst[c] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+  const uint16_t* src = p >= 0 ? x + static_cast<int64_t>(p / k) * d : nullptr;
+  for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (src) {
+      const uint2 w = reinterpret_cast<const uint2*>(src + kb * 128)[lane];
+      v[0] = bf16_lo(w.x);
+      v[1] = bf16_hi(w.x);
+      v[2] = bf16_lo(w.y);
+      v[3] = bf16_hi(w.y);
+    }
+    uint32_t t1, t2, t3;
+    const float inv = warp_split_block(v, t1, t2, t3);
+    warp_store_block(xs, d, xs_inv, R, i, kb, t1, t2, t3, inv, lane);
   }
 }
 
-constexpr int kNormThreads = 256;
-
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_scatter_kernel(
-    const uint16_t* __restrict__ h, const uint16_t* __restrict__ gain, float eps, int32_t d, int32_t k,
-    const int32_t* __restrict__ inv_pos, uint16_t* __restrict__ xs, uint16_t* __restrict__ xs_shared) {
-  __shared__ float red[kNormThreads / 32];
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
+    const uint16_t* __restrict__ h, const uint16_t* __restrict__ gain, float eps, int32_t n, int32_t d, int32_t k,
+    const int32_t* __restrict__ inv_pos, uint8_t* __restrict__ xs, float* __restrict__ xs_inv,
+    uint8_t* __restrict__ xs_shared, float* __restrict__ xs_shared_inv) {
+  __shared__ float red[kRowThreads / 32];
   __shared__ float s_inv;
   const int64_t t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint4* row = reinterpret_cast<const uint4*>(h + t * d);
-  const uint4* g4 = reinterpret_cast<const uint4*>(gain);
   const int nv = d / 8;
   float ss = 0.f;
-  for (int c = threadIdx.x; c < nv; c += kNormThreads) {
+  for (int c = threadIdx.x; c < nv; c += kRowThreads) {
     const uint4 v = row[c];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -79,15 +88,15 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_scatter_kernel(
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  if (lane == 0) red[warp] = ss;
   __syncthreads();
   if (threadIdx.x == 0) {
     float tot = 0.f;
-    for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+    for (int w = 0; w < kRowThreads / 32; ++w) tot += red[w];
     s_inv = rsqrtf(tot / static_cast<float>(d) + eps);
   }
   __syncthreads();
-  const float inv = s_inv;
+  const float inv_rms = s_inv;
 
   int32_t dst_rows[32];
   int ndst = 0;
@@ -95,16 +104,19 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_scatter_kernel(
     const int p = inv_pos[t * k + j];
     if (p >= 0) dst_rows[ndst++] = p;
   }
-  for (int c = threadIdx.x; c < nv; c += kNormThreads) {
-    const uint4 v = row[c], g = g4[c];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      o[q] = pack_f16x2(bf16_lo(gw[q]) * (bf16_lo(w[q]) * inv), bf16_hi(gw[q]) * (bf16_hi(w[q]) * inv));
-    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-    for (int q = 0; q < ndst; ++q) reinterpret_cast<uint4*>(xs + static_cast<int64_t>(dst_rows[q]) * d)[c] = ov;
-    if (xs_shared) reinterpret_cast<uint4*>(xs_shared + t * d)[c] = ov;
+  const int64_t R = static_cast<int64_t>(n) * k;
+  for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
+    const uint2 w = reinterpret_cast<const uint2*>(h + t * d + kb * 128)[lane];
+    const uint2 g = reinterpret_cast<const uint2*>(gain + kb * 128)[lane];
+    float v[4];
+    v[0] = bf16_lo(g.x) * (bf16_lo(w.x) * inv_rms);
+    v[1] = bf16_hi(g.x) * (bf16_hi(w.x) * inv_rms);
+    v[2] = bf16_lo(g.y) * (bf16_lo(w.y) * inv_rms);
+    v[3] = bf16_hi(g.y) * (bf16_hi(w.y) * inv_rms);
+    uint32_t t1, t2, t3;
+    const float inv = warp_split_block(v, t1, t2, t3);
+    for (int q = 0; q < ndst; ++q) warp_store_block(xs, d, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
+    if (xs_shared) warp_store_block(xs_shared, d, xs_shared_inv, n, t, kb, t1, t2, t3, inv, lane);
   }
 }
 
@@ -160,20 +172,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
+// One CTA per tile; tiles enumerated ((expert * rows/128 + row block) * cols/128 + col block).
+__global__ void __launch_bounds__(256) pack_tiles_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                         int32_t rows, int32_t cols) {
+  const int64_t t = blockIdx.x;
+  const int nrb = rows / 128, ncb = cols / 128;
+  const int64_t e = t / (static_cast<int64_t>(nrb) * ncb);
+  const int rem = static_cast<int>(t - e * nrb * ncb);
+  const int b = rem / ncb, c = rem % ncb;
+  const uint8_t* s = src + (e * rows + static_cast<int64_t>(b) * 128) * cols + static_cast<int64_t>(c) * 128;
+  uint8_t* d = dst + t * 16384;
+  for (int q = threadIdx.x; q < 1024; q += 256) {
+    const int r = q >> 3, j = q & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(s + static_cast<int64_t>(r) * cols + j * 16);
+    *reinterpret_cast<uint4*>(d + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+  }
+}
+
 }  // namespace
 
+cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_experts, int32_t rows, int32_t cols,
+                              cudaStream_t s) {
+  const int64_t tiles = static_cast<int64_t>(num_experts) * (rows / 128) * (cols / 128);
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pack_tiles_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(src, dst, rows, cols);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k, int32_t d,
-                               uint16_t* xs_f16, cudaStream_t s) {
+                               uint8_t* xs, float* xs_inv, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
-  gather_rows_kernel<<<R, 128, 0, s>>>(x_bf16, sorted_pos, k, d, xs_f16);
+  gather_rows_kernel<<<R, kRowThreads, 0, s>>>(x_bf16, sorted_pos, R, k, d, xs, xs_inv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_bf16, float eps, int32_t n, int32_t d,
-                                   int32_t k, const int32_t* inv_pos, uint16_t* xs_f16, uint16_t* xs_shared_f16,
-                                   cudaStream_t s) {
+                                   int32_t k, const int32_t* inv_pos, uint8_t* xs, float* xs_inv, uint8_t* xs_shared,
+                                   float* xs_shared_inv, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  rmsnorm_scatter_kernel<<<n, kNormThreads, 0, s>>>(h_bf16, gain_bf16, eps, d, k, inv_pos, xs_f16, xs_shared_f16);
+  rmsnorm_scatter_kernel<<<n, kRowThreads, 0, s>>>(h_bf16, gain_bf16, eps, n, d, k, inv_pos, xs, xs_inv, xs_shared,
+                                                   xs_shared_inv);
   return cudaGetLastError();
 }
 

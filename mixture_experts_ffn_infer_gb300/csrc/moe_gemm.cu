@@ -9,29 +9,28 @@
 // scale per 128 x 128 block.
 //
 // One persistent CTA per SM walks a list of work units.  A unit is one tile of
-// at most kNTok sorted rows of one expert times one block of 128 weight rows
+// at most NTOK sorted rows of one expert times one block of 128 weight rows
 // (128 output features).  The weights are the MMA's M side (128 rows) and the
-// tokens its N side ("swap AB"), so a decode tile of 1-3 tokens still fills
-// the instruction.  Per 128-wide K block:
+// tokens its N side ("swap AB").  The e4m3 weight tiles go from global memory
+// to shared memory by bulk copy (tiled layout) or TMA (row-major layout) and
+// straight into tcgen05.mma kind::f8f6f4 - no conversion.  The activations
+// arrive in the three-term e4m3 split format (split3.cuh): the N side of each
+// MMA holds the three terms of NTOK tokens (N = 3 NTOK).  Per 128-wide K block:
 //
-//   warp 0      TMA producer: e4m3 weight tile(s) 128 x 128 and the f16
-//               activation tile kNTok x 128 into a ring of shared-memory stages.
-//   warps 4-7   converters: thread r owns weight row r; it reads its 128 bytes
-//               (128-byte swizzle), converts e4m3 -> f16 exactly and stores
-//               the row into tensor memory as the MMA's A operand.
-//   warp 1      MMA issuer: 8 x tcgen05.mma kind::f16 (M=128, N=kNTok, K=16),
-//               A from tensor memory, B from shared memory, into a fresh fp32
-//               partial accumulator in tensor memory.
-//   warps 8-11  epilogue: load the partial, multiply it by the block's fp32
-//               scale and add it to fp32 accumulators in registers.  That is
-//               the exact block-scaled product (the scale is constant over the
-//               128 x 128 block), without rounding weight * scale.
+//   warp 0      producer: weight tile(s) 16 KB each + activation block
+//               (3 NTOK rows x 128 bytes) into two rings of stages; L2
+//               prefetch of the weights a few blocks ahead.
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=3 NTOK, K=32) per
+//               matrix into a fresh fp32 partial in tensor memory.
+//   warps 4-7   epilogue: per token, sum the three term columns, multiply by
+//               the weight block's fp32 scale and the activation block's 2^-s
+//               and add to fp32 accumulators in registers - the exact
+//               block-scaled product of the dequantised operands.
 //
 // After the last K block the epilogue writes, per valid token column,
-//   gate/up pass : h = f16(silu(g) * u)            -> h[row][feature]
-//   down pass    : f16(topk_weight * o)            -> rows[flat position][feature]
-// Converted weights never touch shared memory, so shared-memory bandwidth is
-// spent only on the TMA writes, the converters' reads and the small B tiles.
+//   gate/up pass : h = silu(g) * u in the split format (one block scale per
+//                  row and 128 features, found with a max over the 4 warps)
+//   down pass    : f16(topk_weight * o) -> rows[flat position][feature]
 //
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag and
 // the device error word, the roles drain their in-flight copies and MMAs and
@@ -40,15 +39,15 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "split3.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 256;
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
-constexpr int kWarpConv0 = 4;  // warps 4..7 -> tensor-memory lane quarters 0..3
-constexpr int kWarpEpi0 = 8;   // warps 8..11 -> lane quarters 0..3
+constexpr int kWarpEpi0 = 4;  // epilogue: warps 4..7 -> tensor-memory lane quarters 0..3
 
 constexpr int pow2_at_least(int v) {
   int p = 32;
@@ -56,31 +55,40 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int NMAT, int NTOK, int STAGES>
+template <int NMAT, int NTOK, int WST, int BST, int DST>
 struct Cfg {
+  static constexpr int kNB = 3 * NTOK;                   // MMA N: three e4m3 terms per token
   static constexpr int kWTile = 128 * 128;               // e4m3 weight tile bytes
-  static constexpr int kBBox = NTOK * 128;               // one 64-column f16 activation box
-  static constexpr int kStage = NMAT * kWTile + 2 * kBBox;
-  static constexpr int kACols = 64;                      // tensor-memory columns of a converted tile
-  static constexpr int kATotal = 2 * NMAT * kACols;      // two A stages
-  static constexpr int kDTotal = 2 * NMAT * NTOK;        // two partial-accumulator buffers
-  static constexpr int kTmemCols = pow2_at_least(kATotal + kDTotal);
-  static constexpr int kNumBars = 2 * STAGES + 9;
-  static constexpr int kBarBytes = kNumBars * 8 + 16;
-  static constexpr int kSmem = 1024 + STAGES * kStage + kBarBytes;
-  static_assert(kBBox % 1024 == 0, "activation boxes must stay 1024-byte aligned");
+  static constexpr int kWStage = NMAT * kWTile;          // one K block of weights (gate + up, or down)
+  static constexpr int kBStage = kNB * 128;              // one K block of split activations
+  static constexpr int kDCols = NMAT * kNB;              // tensor-memory columns of one partial buffer
+  static constexpr int kTmemCols = pow2_at_least(DST * kDCols);
+  static constexpr int kNumBars = 2 * WST + 2 * BST + 2 * DST + 2 + 1;
+  static constexpr int kBOffset = WST * kWStage;
+  static constexpr int kBarOffset = kBOffset + BST * kBStage;
+  static constexpr int kRedOffset = kBarOffset + kNumBars * 8 + 16;
+  static constexpr int kSmem = 1024 + kRedOffset + 2 * 4 * NTOK * 4;
+  // L2 prefetch runs this many K blocks ahead of the loads (about 128 KB of weights).
+  static constexpr int kPrefetch = (128 * 1024) / kWStage;
+  static_assert(kBStage % 1024 == 0, "activation stages must stay 1024-byte aligned");
   static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
-  static_assert(NTOK % 16 == 0 && NTOK >= 16 && NTOK <= 256, "MMA N for M = 128");
+  static_assert(kNB % 16 == 0 && kNB <= 256, "MMA N for M = 128");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
 struct GemmArgs {
+  const uint8_t* w0_tiled;  // non-null: weights in the tiled layout, streamed with bulk copies
+  const uint8_t* w1_tiled;
   const float* s0;
   const float* s1;
   const TileDesc* tiles;
   const int32_t* n_tiles;
   int32_t n_nb;
   int32_t num_kb;
-  void* out;
+  const float* act_inv;     // [num_kb][act_rows]: 2^-s of each activation block
+  int32_t act_rows;
+  void* out;                // gate/up: h terms [3 act_rows][n_nb*128] e4m3; down: rows [.][n_nb*128] f16
+  float* out_inv;           // gate/up: [n_nb][act_rows] 2^-s of each h block
   const int32_t* sorted_pos;
   const float* topk_weight;
   uint32_t* err;
@@ -93,56 +101,64 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > kWaitLimitCycles) return;
 }
 
-// 16 e4m3 bytes -> 8 words of two f16 each (lower K index in the low half).
-__device__ __forceinline__ void cvt_e4m3x16_f16(const uint4 v, uint32_t* o) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] & 0xffffu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[q] >> 16), __NV_E4M3);
-    o[2 * q] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-    o[2 * q + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-  }
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-template <int NMAT, int NTOK, int STAGES>
+template <int NMAT, int NTOK, int WST, int BST, int DST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                 const __grid_constant__ CUtensorMap tm_act, const GemmArgs a) {
-  using C = Cfg<NMAT, NTOK, STAGES>;
+  using C = Cfg<NMAT, NTOK, WST, BST, DST>;
+  constexpr int NB = C::kNB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + STAGES * C::kStage;
-  auto full = [&](int s) { return bar0 + 8u * s; };
-  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto afull = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
-  auto aempty = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
-  auto dfull = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
-  auto dempty = [&](int i) { return bar0 + 8u * (2 * STAGES + 6 + i); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::kStage + C::kNumBars * 8);
+  const uint32_t bar0 = sbase + C::kBarOffset;
+  // weight ring, activation ring, partial-accumulator buffers
+  auto full_w = [&](int i) { return bar0 + 8u * i; };
+  auto empty_w = [&](int i) { return bar0 + 8u * (WST + i); };
+  auto full_b = [&](int i) { return bar0 + 8u * (2 * WST + i); };
+  auto empty_b = [&](int i) { return bar0 + 8u * (2 * WST + BST + i); };
+  auto dfull = [&](int i) { return bar0 + 8u * (2 * WST + 2 * BST + i); };
+  auto dempty = [&](int i) { return bar0 + 8u * (2 * WST + 2 * BST + DST + i); };
+  auto redbar = [&](int i) { return bar0 + 8u * (2 * WST + 2 * BST + 2 * DST + i); };  // epilogue exchange
+  const uint32_t drain_bar = bar0 + 8u * (C::kNumBars - 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOffset + C::kNumBars * 8);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* red = reinterpret_cast<float*>(smem + C::kRedOffset);  // [2][4 warps][NTOK] block maxima
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), 4 + 1);  // four converter warps + one MMA commit
+    for (int i = 0; i < WST; ++i) {
+      mbar_init(full_w(i), 1);
+      mbar_init(empty_w(i), 1);  // one MMA commit
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(afull(i), 4);
-      mbar_init(aempty(i), 1);
+    for (int i = 0; i < BST; ++i) {
+      mbar_init(full_b(i), 1);
+      mbar_init(empty_b(i), 1);
+    }
+    for (int i = 0; i < DST; ++i) {
       mbar_init(dfull(i), 1);
-      mbar_init(dempty(i), 4);
+      mbar_init(dempty(i), 4);  // the four epilogue warps
     }
+    mbar_init(redbar(0), 4);
+    mbar_init(redbar(1), 4);
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == kWarpProducer && lane == 0) {
-    prefetch_tmap(&tm_w0);
-    if (NMAT == 2) prefetch_tmap(&tm_w1);
+    if (!a.w0_tiled) {
+      prefetch_tmap(&tm_w0);
+      if (NMAT == 2) prefetch_tmap(&tm_w1);
+    }
     prefetch_tmap(&tm_act);
   }
   if (warp == kWarpMma) {
@@ -161,108 +177,109 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      uint32_t it = 0;
+      // L2 prefetch cursor, kPrefetch K blocks ahead of the loads
+      int pf_u = blockIdx.x, pf_kb = 0, pf_e = 0;
+      auto prefetch_one = [&]() {
+        if (pf_u >= total_units) return;
+        if (pf_kb == 0) pf_e = a.tiles[pf_u / n_nb].expert;
+        const int nb = pf_u % n_nb;
+        if (a.w0_tiled) {
+          const int64_t toff = ((static_cast<int64_t>(pf_e) * n_nb + nb) * num_kb + pf_kb) * C::kWTile;
+          bulk_prefetch_l2(a.w0_tiled + toff, C::kWTile);
+          if (NMAT == 2) bulk_prefetch_l2(a.w1_tiled + toff, C::kWTile);
+        } else {
+          tma_prefetch_3d(&tm_w0, pf_kb * 128, nb * 128, pf_e);
+          if (NMAT == 2) tma_prefetch_3d(&tm_w1, pf_kb * 128, nb * 128, pf_e);
+        }
+        if (++pf_kb == num_kb) {
+          pf_kb = 0;
+          pf_u += gridDim.x;
+        }
+      };
+      for (int i = 0; i < C::kPrefetch; ++i) prefetch_one();
+      uint32_t w_issued = 0, b_issued = 0;  // K blocks whose weight / activation loads were issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const TileDesc td = a.tiles[u / n_nb];
         const int nb = u % n_nb;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % STAGES;
-          if (!wait_bounded(empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, a.err)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          const uint32_t it = w_issued;
+          const int sw = it % WST, sb = it % BST;
+          if (!wait_bounded(empty_w(sw), ((it / WST) & 1) ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
-          const uint32_t st = sbase + s * C::kStage;
-          mbar_arrive_expect_tx(full(s), C::kStage);
-          tma_load_3d(st, &tm_w0, full(s), kb * 128, nb * 128, td.expert, pol_w);
-          if (NMAT == 2) tma_load_3d(st + C::kWTile, &tm_w1, full(s), kb * 128, nb * 128, td.expert, pol_w);
-          tma_load_2d(st + NMAT * C::kWTile, &tm_act, full(s), kb * 128, td.row_start, pol_a);
-          tma_load_2d(st + NMAT * C::kWTile + C::kBBox, &tm_act, full(s), kb * 128 + 64, td.row_start, pol_a);
+          const uint32_t wst = sbase + sw * C::kWStage;
+          mbar_arrive_expect_tx(full_w(sw), C::kWStage);
+          if (a.w0_tiled) {  // one contiguous 16 KB block per tile, already in the swizzled image
+            const int64_t toff = ((static_cast<int64_t>(td.expert) * n_nb + nb) * num_kb + kb) * C::kWTile;
+            bulk_load(wst, a.w0_tiled + toff, C::kWTile, full_w(sw), pol_w);
+            if (NMAT == 2) bulk_load(wst + C::kWTile, a.w1_tiled + toff, C::kWTile, full_w(sw), pol_w);
+          } else {
+            tma_load_3d(wst, &tm_w0, full_w(sw), kb * 128, nb * 128, td.expert, pol_w);
+            if (NMAT == 2) tma_load_3d(wst + C::kWTile, &tm_w1, full_w(sw), kb * 128, nb * 128, td.expert, pol_w);
+          }
+          ++w_issued;
+          prefetch_one();
+          if (!wait_bounded(empty_b(sb), ((it / BST) & 1) ^ 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
+          mbar_arrive_expect_tx(full_b(sb), C::kBStage);
+          tma_load_2d(bst, &tm_act, full_b(sb), kb * 128, td.row_start * 3, pol_a);
+          ++b_issued;
         }
       }
-      if (!ok)  // wait for the copies already in flight before the CTA exits
-        for (uint32_t i = it > STAGES ? it - STAGES : 0; i < it; ++i) wait_drain(full(i % STAGES), (i / STAGES) & 1);
+      if (!ok) {  // wait for the copies already in flight before the CTA exits
+        for (uint32_t i = w_issued > WST ? w_issued - WST : 0; i < w_issued; ++i)
+          wait_drain(full_w(i % WST), (i / WST) & 1);
+        for (uint32_t i = b_issued > BST ? b_issued - BST : 0; i < b_issued; ++i)
+          wait_drain(full_b(i % BST), (i / BST) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(128, NTOK);
+      constexpr uint32_t idesc = idesc_f16_f32(128, NB);  // kind::f8f6f4: E4M3 has format code 0, as f16
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % STAGES;
-          const int sa = it & 1;
-          const uint32_t pa = (it >> 1) & 1;
-          if (!wait_bounded(full(s), (it / STAGES) & 1, abort_flag, a.err) ||
-              !wait_bounded(afull(sa), pa, abort_flag, a.err) ||
-              !wait_bounded(dempty(sa), pa ^ 1, abort_flag, a.err)) {
+          const int sw = it % WST, sb = it % BST, sd = it % DST;
+          if (!wait_bounded(full_w(sw), (it / WST) & 1, abort_flag, a.err) ||
+              !wait_bounded(full_b(sb), (it / BST) & 1, abort_flag, a.err) ||
+              !wait_bounded(dempty(sd), ((it / DST) & 1) ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bst = sbase + s * C::kStage + NMAT * C::kWTile;
+          const uint32_t wst = sbase + sw * C::kWStage;
+          const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
 #pragma unroll
           for (int m = 0; m < NMAT; ++m) {
-            const uint32_t d_addr = tmem + C::kATotal + (sa * NMAT + m) * NTOK;
-            const uint32_t a_addr = tmem + (sa * NMAT + m) * C::kACols;
+            const uint32_t d_addr = tmem + (sd * NMAT + m) * NB;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t baddr = bst + (kk >> 2) * C::kBBox + (kk & 3) * 32;
-              mma_f16_ts(d_addr, a_addr + kk * 8, desc_kmajor_sw128(baddr), idesc, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8_ss(d_addr, desc_kmajor_sw128(wst + m * C::kWTile + kk * 32), desc_kmajor_sw128(bst + kk * 32),
+                        idesc, kk > 0 ? 1u : 0u);
           }
-          tc_commit(aempty(sa));
-          tc_commit(empty(s));
-          tc_commit(dfull(sa));
+          tc_commit(empty_w(sw));
+          tc_commit(empty_b(sb));
+          tc_commit(dfull(sd));
         }
       }
       tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
       wait_drain(drain_bar, 0);
     }
     __syncwarp();
-  } else if (warp >= kWarpConv0 && warp < kWarpConv0 + 4) {
-    const int q = warp - kWarpConv0;
-    const int r = q * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
-        const int s = it % STAGES;
-        const int sa = it & 1;
-        // Every lane waits (each gets the barrier's acquire); the vote keeps the
-        // warp converged for the .sync.aligned tensor-memory stores.
-        ok = __all_sync(0xffffffffu, wait_bounded(full(s), (it / STAGES) & 1, abort_flag, a.err) &&
-                                         wait_bounded(aempty(sa), ((it >> 1) & 1) ^ 1, abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint32_t row = sbase + s * C::kStage + m * C::kWTile + r * 128;
-          uint32_t v[64];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) cvt_e4m3x16_f16(lds128(row + ((c ^ (r & 7)) << 4)), v + 8 * c);
-          const uint32_t taddr = tmem + lane_base + (sa * NMAT + m) * C::kACols;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tmem_st16(taddr + 16 * j, v + 16 * j);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(afull(sa));
-          mbar_arrive(empty(s));
-        }
-      }
-    }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
     const int q = warp - kWarpEpi0;
     const int r = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t it = 0;
+    uint32_t it = 0, ui = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
       const TileDesc td = a.tiles[u / n_nb];
       const int nb = u % n_nb;
       const float* sc0 = a.s0 + (static_cast<int64_t>(td.expert) * n_nb + nb) * num_kb;
@@ -273,42 +290,71 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) acc[m][j] = 0.f;
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
-        const int sd = it & 1;
+        const int sd = it % DST;
         const float s0v = __ldg(sc0 + kb);
         const float s1v = NMAT == 2 ? __ldg(sc1 + kb) : 0.f;
-        ok = __all_sync(0xffffffffu, wait_bounded(dfull(sd), (it >> 1) & 1, abort_flag, a.err));
+        float sx[NTOK];  // 2^-s of each token's activation block
+        const float* inv = a.act_inv + static_cast<int64_t>(kb) * a.act_rows + td.row_start;
+#pragma unroll
+        for (int j = 0; j < NTOK; ++j) sx[j] = j < td.n_valid ? __ldg(inv + j) : 0.f;
+        ok = __all_sync(0xffffffffu, wait_bounded(dfull(sd), (it / DST) & 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
-        uint32_t p[NMAT][NTOK];
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m)
+        for (int m = 0; m < NMAT; ++m) {
+          const float sv = m == 0 ? s0v : s1v;
+          uint32_t p[NB];
 #pragma unroll
-          for (int j0 = 0; j0 < NTOK; j0 += 16)
-            tmem_ld16(tmem + lane_base + C::kATotal + (sd * NMAT + m) * NTOK + j0,
-                      *reinterpret_cast<uint32_t(*)[16]>(&p[m][j0]));
-        tmem_ld_wait();
+          for (int c0 = 0; c0 < NB; c0 += 16)
+            tmem_ld16(tmem + lane_base + (sd * NMAT + m) * NB + c0, *reinterpret_cast<uint32_t(*)[16]>(&p[c0]));
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < NTOK; ++j) {
+            const float part = (__uint_as_float(p[3 * j]) + __uint_as_float(p[3 * j + 1])) +
+                               __uint_as_float(p[3 * j + 2]);
+            acc[m][j] = fmaf(sv * sx[j], part, acc[m][j]);
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dempty(sd));
-#pragma unroll
-        for (int j = 0; j < NTOK; ++j) {
-          acc[0][j] = fmaf(s0v, __uint_as_float(p[0][j]), acc[0][j]);
-          if (NMAT == 2) acc[NMAT - 1][j] = fmaf(s1v, __uint_as_float(p[NMAT - 1][j]), acc[NMAT - 1][j]);
-        }
       }
       if (!ok) break;
       bool overflow = false;
       if (NMAT == 2) {
-        uint16_t* h = static_cast<uint16_t*>(a.out);
+        // h = silu(g) * u, then the split format with one exponent per (row, 128 features):
+        // the block maximum is taken over the 128 threads (4 warps x 32 lanes).
+        // The exchange goes through red[ui & 1] and an mbarrier of four arrivals, so a
+        // warp can be one unit ahead of the others and every wait stays bounded.
+        float* rb = red + (ui & 1) * 4 * NTOK;
+        float hv[NTOK];
+#pragma unroll
+        for (int j = 0; j < NTOK; ++j) {
+          const float g = acc[0][j];
+          hv[j] = g / (1.0f + expf(-g)) * acc[NMAT - 1][j];
+          overflow |= (j < td.n_valid) && !isfinite(hv[j]);
+          const float m = warp_max(fabsf(hv[j]));
+          if (lane == 0) rb[q * NTOK + j] = m;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(redbar(ui & 1));
+        ok = __all_sync(0xffffffffu, wait_bounded(redbar(ui & 1), (ui >> 1) & 1, abort_flag, a.err));
+        if (!ok) break;
+        uint8_t* hterm = static_cast<uint8_t*>(a.out);
         const int64_t ld = static_cast<int64_t>(n_nb) * 128;
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) {
           if (j < td.n_valid) {
-            const float g = acc[0][j], uu = acc[NMAT - 1][j];
-            const float hv = g / (1.0f + expf(-g)) * uu;
-            const __half hh = __float2half_rn(hv);
-            overflow |= __hisinf(hh) != 0 || __hisnan(hh);
-            h[static_cast<int64_t>(td.row_start + j) * ld + nb * 128 + r] = __half_as_ushort(hh);
+            const float m = fmaxf(fmaxf(rb[j], rb[NTOK + j]), fmaxf(rb[2 * NTOK + j], rb[3 * NTOK + j]));
+            const int sexp = split_exponent(m);
+            uint8_t t1, t2, t3;
+            split3(ldexpf(hv[j], sexp), t1, t2, t3);
+            const int64_t row = td.row_start + j;
+            uint8_t* dst = hterm + (3 * row) * ld + nb * 128 + r;
+            dst[0] = t1;
+            dst[ld] = t2;
+            dst[2 * ld] = t3;
+            if (r == 0) a.out_inv[static_cast<int64_t>(nb) * a.act_rows + row] = ldexpf(1.0f, -sexp);
           }
         }
       } else {
@@ -336,20 +382,25 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   }
 }
 
-template <int NMAT, int NTOK, int STAGES>
+template <int NMAT, int NTOK, int WST, int BST, int DST>
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  using C = Cfg<NMAT, NTOK, STAGES>;
-  auto kern = moe_gemm_kernel<NMAT, NTOK, STAGES>;
+  using C = Cfg<NMAT, NTOK, WST, BST, DST>;
+  auto kern = moe_gemm_kernel<NMAT, NTOK, WST, BST, DST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   GemmArgs a;
+  a.w0_tiled = g.w0_tiled;
+  a.w1_tiled = g.w1_tiled;
   a.s0 = g.s0;
   a.s1 = g.s1;
   a.tiles = g.tiles;
   a.n_tiles = g.n_tiles;
   a.n_nb = g.n_nb;
   a.num_kb = g.num_kb;
+  a.act_inv = g.act_inv;
+  a.act_rows = g.act_rows;
   a.out = g.out;
+  a.out_inv = g.out_inv;
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;
@@ -359,7 +410,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<2, kNTok, 6>(g, s); }
-cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 10>(g, s); }
+// gate/up: 6 x 32 KB weight stages, 4 x 6 KB activation stages, 4 partial buffers (384 columns)
+cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<2, kNTok, 6, 4, 4>(g, s); }
+// down: 12 x 16 KB weight stages, 4 x 6 KB activation stages, 4 partial buffers (192 columns)
+cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 12, 4, 4>(g, s); }
 
 }  // namespace moe
