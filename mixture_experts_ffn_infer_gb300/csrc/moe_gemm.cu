@@ -17,9 +17,10 @@
 // arrive in the three-term e4m3 split format (split3.cuh): the N side of each
 // MMA holds the three terms of NTOK tokens (N = 3 NTOK).  Per 128-wide K block:
 //
-//   warp 0      producer: weight tile(s) 16 KB each + activation block
-//               (3 NTOK rows x 128 bytes) into two rings of stages; L2
-//               prefetch of the weights a few blocks ahead.
+//   warp 0      weight producer: tile(s) of 16 KB into a ring of stages, L2
+//               prefetch a few blocks ahead.
+//   warp 2      activation producer: the block of 3 NTOK rows x 128 bytes
+//               into its own ring, so neither ring throttles the other.
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=3 NTOK, K=32) per
 //               matrix into a fresh fp32 partial in tensor memory.
 //   warps 4-7   epilogue: per token, sum the three term columns, multiply by
@@ -45,9 +46,10 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarpProducer = 0;
+constexpr int kWarpProducer = 0;     // weight loads and L2 prefetch
 constexpr int kWarpMma = 1;
-constexpr int kWarpEpi0 = 4;  // epilogue: warps 4..7 -> tensor-memory lane quarters 0..3
+constexpr int kWarpActProducer = 2;  // activation loads
+constexpr int kWarpEpi0 = 4;         // epilogue: warps 4..7 -> tensor-memory lane quarters 0..3
 
 constexpr int pow2_at_least(int v) {
   int p = 32;
@@ -176,7 +178,6 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   if (warp == kWarpProducer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
       // L2 prefetch cursor, kPrefetch K blocks ahead of the loads
       int pf_u = blockIdx.x, pf_kb = 0, pf_e = 0;
       auto prefetch_one = [&]() {
@@ -197,14 +198,14 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         }
       };
       for (int i = 0; i < C::kPrefetch; ++i) prefetch_one();
-      uint32_t w_issued = 0, b_issued = 0;  // K blocks whose weight / activation loads were issued
+      uint32_t w_issued = 0;  // K blocks whose weight loads were issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const TileDesc td = a.tiles[u / n_nb];
+        const int e = a.tiles[u / n_nb].expert;
         const int nb = u % n_nb;
         for (int kb = 0; kb < num_kb; ++kb) {
           const uint32_t it = w_issued;
-          const int sw = it % WST, sb = it % BST;
+          const int sw = it % WST;
           if (!wait_bounded(empty_w(sw), ((it / WST) & 1) ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
@@ -212,31 +213,45 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
           const uint32_t wst = sbase + sw * C::kWStage;
           mbar_arrive_expect_tx(full_w(sw), C::kWStage);
           if (a.w0_tiled) {  // one contiguous 16 KB block per tile, already in the swizzled image
-            const int64_t toff = ((static_cast<int64_t>(td.expert) * n_nb + nb) * num_kb + kb) * C::kWTile;
+            const int64_t toff = ((static_cast<int64_t>(e) * n_nb + nb) * num_kb + kb) * C::kWTile;
             bulk_load(wst, a.w0_tiled + toff, C::kWTile, full_w(sw), pol_w);
             if (NMAT == 2) bulk_load(wst + C::kWTile, a.w1_tiled + toff, C::kWTile, full_w(sw), pol_w);
           } else {
-            tma_load_3d(wst, &tm_w0, full_w(sw), kb * 128, nb * 128, td.expert, pol_w);
-            if (NMAT == 2) tma_load_3d(wst + C::kWTile, &tm_w1, full_w(sw), kb * 128, nb * 128, td.expert, pol_w);
+            tma_load_3d(wst, &tm_w0, full_w(sw), kb * 128, nb * 128, e, pol_w);
+            if (NMAT == 2) tma_load_3d(wst + C::kWTile, &tm_w1, full_w(sw), kb * 128, nb * 128, e, pol_w);
           }
           ++w_issued;
           prefetch_one();
+        }
+      }
+      if (!ok)  // wait for the copies already in flight before the CTA exits
+        for (uint32_t i = w_issued > WST ? w_issued - WST : 0; i < w_issued; ++i)
+          wait_drain(full_w(i % WST), (i / WST) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kWarpActProducer) {
+    if (lane == 0) {
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t b_issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const int row0 = a.tiles[u / n_nb].row_start;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          const uint32_t it = b_issued;
+          const int sb = it % BST;
           if (!wait_bounded(empty_b(sb), ((it / BST) & 1) ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
           const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
           mbar_arrive_expect_tx(full_b(sb), C::kBStage);
-          tma_load_2d(bst, &tm_act, full_b(sb), kb * 128, td.row_start * 3, pol_a);
+          tma_load_2d(bst, &tm_act, full_b(sb), kb * 128, row0 * 3, pol_a);
           ++b_issued;
         }
       }
-      if (!ok) {  // wait for the copies already in flight before the CTA exits
-        for (uint32_t i = w_issued > WST ? w_issued - WST : 0; i < w_issued; ++i)
-          wait_drain(full_w(i % WST), (i / WST) & 1);
+      if (!ok)
         for (uint32_t i = b_issued > BST ? b_issued - BST : 0; i < b_issued; ++i)
           wait_drain(full_b(i % BST), (i / BST) & 1);
-      }
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -289,14 +304,38 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       for (int m = 0; m < NMAT; ++m)
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) acc[m][j] = 0.f;
+      // Down pass: destination rows and router weights of the tile, loaded now so their
+      // latency hides behind the K loop instead of stalling the end of the unit.
+      int dest[NMAT == 1 ? NTOK : 1];
+      float wgt[NMAT == 1 ? NTOK : 1];
+      if (NMAT == 1) {
+#pragma unroll
+        for (int j = 0; j < NTOK; ++j) {
+          const int row = td.row_start + j;
+          dest[j] = j < td.n_valid ? (a.sorted_pos ? __ldg(a.sorted_pos + row) : row) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < NTOK; ++j)
+          wgt[j] = (j < td.n_valid && a.topk_weight) ? __ldg(a.topk_weight + dest[j]) : 1.0f;
+      }
+      // scales of the first K block; each iteration loads the next block's
+      float s0n = __ldg(sc0), s1n = NMAT == 2 ? __ldg(sc1) : 0.f;
+      float sxn[NTOK];
+#pragma unroll
+      for (int j = 0; j < NTOK; ++j) sxn[j] = j < td.n_valid ? __ldg(a.act_inv + td.row_start + j) : 0.f;
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int sd = it % DST;
-        const float s0v = __ldg(sc0 + kb);
-        const float s1v = NMAT == 2 ? __ldg(sc1 + kb) : 0.f;
+        const float s0v = s0n, s1v = s1n;
         float sx[NTOK];  // 2^-s of each token's activation block
-        const float* inv = a.act_inv + static_cast<int64_t>(kb) * a.act_rows + td.row_start;
 #pragma unroll
-        for (int j = 0; j < NTOK; ++j) sx[j] = j < td.n_valid ? __ldg(inv + j) : 0.f;
+        for (int j = 0; j < NTOK; ++j) sx[j] = sxn[j];
+        if (kb + 1 < num_kb) {
+          s0n = __ldg(sc0 + kb + 1);
+          if (NMAT == 2) s1n = __ldg(sc1 + kb + 1);
+          const float* inv = a.act_inv + static_cast<int64_t>(kb + 1) * a.act_rows + td.row_start;
+#pragma unroll
+          for (int j = 0; j < NTOK; ++j) sxn[j] = j < td.n_valid ? __ldg(inv + j) : 0.f;
+        }
         ok = __all_sync(0xffffffffu, wait_bounded(dfull(sd), (it / DST) & 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
@@ -363,12 +402,9 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) {
           if (j < td.n_valid) {
-            const int row = td.row_start + j;
-            const int dest = a.sorted_pos ? a.sorted_pos[row] : row;
-            const float w = a.topk_weight ? a.topk_weight[dest] : 1.0f;
-            const __half hh = __float2half_rn(acc[0][j] * w);
+            const __half hh = __float2half_rn(acc[0][j] * wgt[NMAT == 1 ? j : 0]);
             overflow |= __hisinf(hh) != 0 || __hisnan(hh);
-            rows[static_cast<int64_t>(dest) * ld + nb * 128 + r] = __half_as_ushort(hh);
+            rows[static_cast<int64_t>(dest[NMAT == 1 ? j : 0]) * ld + nb * 128 + r] = __half_as_ushort(hh);
           }
         }
       }
@@ -412,7 +448,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 
 // gate/up: 6 x 32 KB weight stages, 4 x 6 KB activation stages, 4 partial buffers (384 columns)
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<2, kNTok, 6, 4, 4>(g, s); }
-// down: 12 x 16 KB weight stages, 4 x 6 KB activation stages, 4 partial buffers (192 columns)
-cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 12, 4, 4>(g, s); }
+// down: 12 x 16 KB weight stages, 4 x 6 KB activation stages, 8 partial buffers (384 columns)
+cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 12, 4, 8>(g, s); }
 
 }  // namespace moe
