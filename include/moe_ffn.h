@@ -186,6 +186,33 @@ moe_status moe_layer_forward(const moe_dims *dims, int64_t n_tokens, const void 
                              void *out, int32_t out_is_fp32, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream, moe_trace *trace);
 
+/* moe_infer without a workspace, for callers that cannot allocate device
+ * memory themselves: code that only receives input and output buffers from a
+ * host framework (a plugin or an embedded runtime with its own memory
+ * planner), code running inside another library's allocator or memory hooks,
+ * and latency-critical paths where a cudaMalloc could synchronise the device.
+ * The pages have no counterpart; it is a packaging of moe_infer.
+ *   Scratch: a fixed array of MOE_STATIC_SCRATCH_BYTES inside this library,
+ *   reserved on every GPU that loads it until the process exits.  Problems
+ *   whose moe_workspace_size(dims, n, 0) exceeds it are rejected with
+ *   MOE_ERR_WORKSPACE before anything runs (at K2 sizes, d 7168 / d_ff 2048 /
+ *   k 8, that allows up to 24 tokens).
+ *   Set-up: the first call on each device looks the array's device address up
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  No call allocates or frees memory.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents; calls that can overlap on the GPU (different streams
+ *   without ordering, several host threads) race and corrupt each other's
+ *   results, so order them.
+ *   Errors: host-detectable errors are returned as by moe_infer.  Device-
+ *   detected errors (bad expert ids, timeouts, f16 overflow) land in the shared
+ *   array and are not reported; use moe_infer with a workspace to read them.
+ * Arguments are those of moe_infer without workspace and trace. */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+moe_status moe_infer_static(const moe_dims *dims, int64_t n_tokens, const void *x, const int32_t *topk_ids,
+                            const float *topk_weight, const moe_weights *weights, void *out, int32_t out_is_fp32,
+                            cudaStream_t stream);
+
 /* Synchronises `stream`, returns the first device-detected error recorded in
  * `workspace` since the last call (MOE_OK if none) and clears it. */
 moe_status moe_get_error(void *workspace, cudaStream_t stream);

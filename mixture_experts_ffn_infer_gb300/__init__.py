@@ -77,8 +77,12 @@ _SIGS = {
                                          ctypes.POINTER(moe_weights), ctypes.POINTER(moe_weights), ctypes.c_int32,
                                          ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
                                          ctypes.c_void_p, ctypes.POINTER(moe_trace)]),
+    "moe_infer_static": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 3
+                         + [ctypes.POINTER(moe_weights), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "moe_get_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
 }
+
+MOE_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 def load_library(path: Optional[str] = None):
@@ -189,6 +193,13 @@ def moe_layer_forward(dm, n_tokens, hidden, gain, eps, topk_ids, topk_weight, ro
                                           ws.numel() * ws.element_size(), _stream(stream),
                                           ctypes.byref(trace) if trace is not None else None)
     _check(st, "moe_layer_forward")
+
+
+def moe_infer_static(dm, n_tokens, x, topk_ids, topk_weight, w: moe_weights, out, out_is_fp32=False, stream=None):
+    """moe_infer on the library's built-in scratch (no workspace argument)."""
+    st = load_library().moe_infer_static(ctypes.byref(dm), n_tokens, _ptr(x), _ptr(topk_ids), _ptr(topk_weight),
+                                         ctypes.byref(w), _ptr(out), int(bool(out_is_fp32)), _stream(stream))
+    _check(st, "moe_infer_static")
 
 
 def moe_get_error(ws, stream=None) -> int:

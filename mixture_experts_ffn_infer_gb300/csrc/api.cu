@@ -296,6 +296,34 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
 }  // namespace
 }  // namespace moe
 
+// Scratch of moe_infer_static: a fixed device array in this library, so that
+// entry point needs no workspace from its caller.  Every GPU that loads the
+// library reserves it until the process exits.  Host code must not pass the
+// symbol itself to a kernel (on the host it only names a stand-in object); the
+// device address comes from cudaGetSymbolAddress below.
+#define MOE_STATIC_SCRATCH_BYTES_VALUE (size_t(8) << 20)
+static __device__ __align__(256) uint8_t moe_static_scratch[MOE_STATIC_SCRATCH_BYTES_VALUE];
+
+namespace {
+
+// Device address of moe_static_scratch on the current device, looked up once per
+// device (with that device current) and remembered; nullptr if the lookup fails.
+void* static_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, moe_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
 using namespace moe;
 
 extern "C" {
@@ -457,6 +485,22 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
                                 static_cast<int32_t>(n), dims->top_k, dims->d, out, out_is_fp32, s));
   tr.after("combine");
   return MOE_OK;
+}
+
+moe_status moe_infer_static(const moe_dims* dims, int64_t n, const void* x, const int32_t* topk_ids,
+                            const float* topk_weight, const moe_weights* w, void* out, int32_t out_is_fp32,
+                            cudaStream_t s) {
+  if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (L.total > MOE_STATIC_SCRATCH_BYTES_VALUE) return MOE_ERR_WORKSPACE;  // problem too big for the scratch
+  if (n == 0) return MOE_OK;
+  void* ws = static_scratch_address();
+  if (!ws) return MOE_ERR_CUDA;
+  // The same sequence as moe_infer; its first kernel resets the error word, the
+  // only part of the scratch that must start at zero.
+  return moe_infer(dims, n, x, topk_ids, topk_weight, w, out, out_is_fp32, ws, MOE_STATIC_SCRATCH_BYTES_VALUE, s,
+                   nullptr);
 }
 
 moe_status moe_get_error(void* ws, cudaStream_t s) {
