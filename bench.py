@@ -112,6 +112,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the GEMM source
+    has changed since those counters were taken."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    src = os.path.join(ROOT, "mixture_experts_ffn_infer_gb300", "csrc", "moe_gemm.cu")
+    try:
+        rec = json.load(open(prof))
+        if rec.get("source_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
+            return None
+        return rec.get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------------------- algorithmic cost
 
 def algorithmic(wl, ids_list, n_tokens):
@@ -276,13 +291,7 @@ def run_ours(args, rank, world, local_rank):
     step_roof_ms = alg["step_bytes"] / (hbm * 1e9) * 1e3
     bf16, bf16_src = _bf16_peak(sustained=True)
     tflops = alg["step_flops"] / (ms_step / 1e3) / 1e12
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get(dominant)
-        except (OSError, ValueError):
-            traffic = None
+    traffic = _traffic(args.workload, dominant)
     result = {
         "metric": METRIC,
         "value": value,
@@ -307,6 +316,13 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": hbm_src + " (MEASURED_PEAKS.json hbm_gbs)" if hbm_src == "measured" else hbm_src,
                      "unit": "GB/s", "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
                      "alg_bytes_per_launch": alg["gateup_bytes"], "kernel_ms": dom_ms},
+        "down_roofline": {"kernel": "down_scatter", "kernel_ms": kern_ms.get("down_scatter"),
+                          "alg_bytes_per_launch": alg["down_bytes"],
+                          "achieved": (alg["down_bytes"] / (kern_ms["down_scatter"] / 1e3) / 1e9)
+                          if kern_ms.get("down_scatter") else None,
+                          "frac": (alg["down_bytes"] / (kern_ms["down_scatter"] / 1e3) / 1e9 / hbm)
+                          if kern_ms.get("down_scatter") else None,
+                          "traffic": _traffic(args.workload, "down_scatter")},
         "step_roofline": {"bytes": alg["step_bytes"], "flops": alg["step_flops"], "t_roof_ms_hbm": step_roof_ms,
                           "frac_hbm": step_roof_ms / ms_step, "tflops": tflops,
                           "frac_bf16_sustained": tflops / bf16, "bf16_peak_source": bf16_src},
@@ -360,7 +376,7 @@ class _Sparse:
 def cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=20.0):
     # sample: the first tokens of the batch; one probe token sizes the sample to the budget
     rate1, _, dt1, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, 1, budget_s)
-    n_tok = max(1, min(8 * x.shape[0], int(budget_s / max(dt1, 1e-3) * max(1, threads // 2))))
+    n_tok = max(1, min(4096, int(budget_s / max(dt1, 1e-3) * max(1, threads))))
     rate, n_tok, dt, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s)
     return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{n_tok} token evaluations cycling over the {x.shape[0]}-token {wl.name} batch "
@@ -422,8 +438,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="k2_decode",
                     choices=["tiny", "k2_decode", "k2_prefill", "k2_skewed", "k2_block"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -57,11 +57,12 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int NMAT, int NTOK, int WST, int BST, int DST>
+template <int NMAT, int NTOK, int KPS, int WST, int BST, int DST>
 struct Cfg {
   static constexpr int kNB = 3 * NTOK;                   // MMA N: three e4m3 terms per token
   static constexpr int kWTile = 128 * 128;               // e4m3 weight tile bytes
-  static constexpr int kWStage = NMAT * kWTile;          // one K block of weights (gate + up, or down)
+  static constexpr int kWMat = KPS * kWTile;             // KPS consecutive K blocks of one matrix
+  static constexpr int kWStage = NMAT * kWMat;           // one weight stage (gate + up, or down)
   static constexpr int kBStage = kNB * 128;              // one K block of split activations
   static constexpr int kDCols = NMAT * kNB;              // tensor-memory columns of one partial buffer
   static constexpr int kTmemCols = pow2_at_least(DST * kDCols);
@@ -70,7 +71,7 @@ struct Cfg {
   static constexpr int kBarOffset = kBOffset + BST * kBStage;
   static constexpr int kRedOffset = kBarOffset + kNumBars * 8 + 16;
   static constexpr int kSmem = 1024 + kRedOffset + 2 * 4 * NTOK * 4;
-  // L2 prefetch runs this many K blocks ahead of the loads (about 128 KB of weights).
+  // L2 prefetch runs this many weight stages ahead of the loads (about 128 KB).
   static constexpr int kPrefetch = (128 * 1024) / kWStage;
   static_assert(kBStage % 1024 == 0, "activation stages must stay 1024-byte aligned");
   static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
@@ -113,11 +114,11 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-template <int NMAT, int NTOK, int WST, int BST, int DST>
+template <int NMAT, int NTOK, int KPS, int WST, int BST, int DST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                 const __grid_constant__ CUtensorMap tm_act, const GemmArgs a) {
-  using C = Cfg<NMAT, NTOK, WST, BST, DST>;
+  using C = Cfg<NMAT, NTOK, KPS, WST, BST, DST>;
   constexpr int NB = C::kNB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -178,47 +179,57 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   if (warp == kWarpProducer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      // L2 prefetch cursor, kPrefetch K blocks ahead of the loads
+      // L2 prefetch cursor, kPrefetch stages ahead of the loads
       int pf_u = blockIdx.x, pf_kb = 0, pf_e = 0;
       auto prefetch_one = [&]() {
         if (pf_u >= total_units) return;
         if (pf_kb == 0) pf_e = a.tiles[pf_u / n_nb].expert;
         const int nb = pf_u % n_nb;
+        const int nk = min(KPS, num_kb - pf_kb);
         if (a.w0_tiled) {
           const int64_t toff = ((static_cast<int64_t>(pf_e) * n_nb + nb) * num_kb + pf_kb) * C::kWTile;
-          bulk_prefetch_l2(a.w0_tiled + toff, C::kWTile);
-          if (NMAT == 2) bulk_prefetch_l2(a.w1_tiled + toff, C::kWTile);
+          bulk_prefetch_l2(a.w0_tiled + toff, nk * C::kWTile);
+          if (NMAT == 2) bulk_prefetch_l2(a.w1_tiled + toff, nk * C::kWTile);
         } else {
-          tma_prefetch_3d(&tm_w0, pf_kb * 128, nb * 128, pf_e);
-          if (NMAT == 2) tma_prefetch_3d(&tm_w1, pf_kb * 128, nb * 128, pf_e);
+          for (int j = 0; j < nk; ++j) {
+            tma_prefetch_3d(&tm_w0, (pf_kb + j) * 128, nb * 128, pf_e);
+            if (NMAT == 2) tma_prefetch_3d(&tm_w1, (pf_kb + j) * 128, nb * 128, pf_e);
+          }
         }
-        if (++pf_kb == num_kb) {
+        pf_kb += nk;
+        if (pf_kb == num_kb) {
           pf_kb = 0;
           pf_u += gridDim.x;
         }
       };
       for (int i = 0; i < C::kPrefetch; ++i) prefetch_one();
-      uint32_t w_issued = 0;  // K blocks whose weight loads were issued
+      uint32_t w_issued = 0;  // weight stages issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const int e = a.tiles[u / n_nb].expert;
         const int nb = u % n_nb;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < num_kb; kb += KPS) {
           const uint32_t it = w_issued;
           const int sw = it % WST;
+          const int nk = min(KPS, num_kb - kb);
           if (!wait_bounded(empty_w(sw), ((it / WST) & 1) ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
           const uint32_t wst = sbase + sw * C::kWStage;
-          mbar_arrive_expect_tx(full_w(sw), C::kWStage);
-          if (a.w0_tiled) {  // one contiguous 16 KB block per tile, already in the swizzled image
+          mbar_arrive_expect_tx(full_w(sw), NMAT * nk * C::kWTile);
+          if (a.w0_tiled) {
+            // the stage's K blocks are consecutive 16 KB tiles, already in the swizzled
+            // image: one bulk copy of up to KPS tiles per matrix
             const int64_t toff = ((static_cast<int64_t>(e) * n_nb + nb) * num_kb + kb) * C::kWTile;
-            bulk_load(wst, a.w0_tiled + toff, C::kWTile, full_w(sw), pol_w);
-            if (NMAT == 2) bulk_load(wst + C::kWTile, a.w1_tiled + toff, C::kWTile, full_w(sw), pol_w);
+            bulk_load(wst, a.w0_tiled + toff, nk * C::kWTile, full_w(sw), pol_w);
+            if (NMAT == 2) bulk_load(wst + C::kWMat, a.w1_tiled + toff, nk * C::kWTile, full_w(sw), pol_w);
           } else {
-            tma_load_3d(wst, &tm_w0, full_w(sw), kb * 128, nb * 128, e, pol_w);
-            if (NMAT == 2) tma_load_3d(wst + C::kWTile, &tm_w1, full_w(sw), kb * 128, nb * 128, e, pol_w);
+            for (int j = 0; j < nk; ++j) {
+              tma_load_3d(wst + j * C::kWTile, &tm_w0, full_w(sw), (kb + j) * 128, nb * 128, e, pol_w);
+              if (NMAT == 2)
+                tma_load_3d(wst + C::kWMat + j * C::kWTile, &tm_w1, full_w(sw), (kb + j) * 128, nb * 128, e, pol_w);
+            }
           }
           ++w_issued;
           prefetch_one();
@@ -257,31 +268,39 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   } else if (warp == kWarpMma) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(128, NB);  // kind::f8f6f4: E4M3 has format code 0, as f16
-      uint32_t it = 0;
+      uint32_t it = 0, wt = 0;  // K blocks and weight stages consumed
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int sw = it % WST, sb = it % BST, sd = it % DST;
-          if (!wait_bounded(full_w(sw), (it / WST) & 1, abort_flag, a.err) ||
-              !wait_bounded(full_b(sb), (it / BST) & 1, abort_flag, a.err) ||
-              !wait_bounded(dempty(sd), ((it / DST) & 1) ^ 1, abort_flag, a.err)) {
+        for (int kb0 = 0; ok && kb0 < num_kb; kb0 += KPS, ++wt) {
+          const int sw = wt % WST;
+          const int nk = min(KPS, num_kb - kb0);
+          if (!wait_bounded(full_w(sw), (wt / WST) & 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint32_t wst = sbase + sw * C::kWStage;
-          const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
+          for (int j = 0; j < nk; ++j, ++it) {
+            const int sb = it % BST, sd = it % DST;
+            if (!wait_bounded(full_b(sb), (it / BST) & 1, abort_flag, a.err) ||
+                !wait_bounded(dempty(sd), ((it / DST) & 1) ^ 1, abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
 #pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            const uint32_t d_addr = tmem + (sd * NMAT + m) * NB;
+            for (int m = 0; m < NMAT; ++m) {
+              const uint32_t d_addr = tmem + (sd * NMAT + m) * NB;
+              const uint32_t wtile = wst + m * C::kWMat + j * C::kWTile;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8_ss(d_addr, desc_kmajor_sw128(wst + m * C::kWTile + kk * 32), desc_kmajor_sw128(bst + kk * 32),
-                        idesc, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ss(d_addr, desc_kmajor_sw128(wtile + kk * 32), desc_kmajor_sw128(bst + kk * 32), idesc,
+                          kk > 0 ? 1u : 0u);
+            }
+            tc_commit(empty_b(sb));
+            tc_commit(dfull(sd));
           }
-          tc_commit(empty_w(sw));
-          tc_commit(empty_b(sb));
-          tc_commit(dfull(sd));
+          if (ok) tc_commit(empty_w(sw));  // the stage's weights are free once its MMAs complete
         }
       }
       tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
@@ -418,10 +437,10 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   }
 }
 
-template <int NMAT, int NTOK, int WST, int BST, int DST>
+template <int NMAT, int NTOK, int KPS, int WST, int BST, int DST>
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  using C = Cfg<NMAT, NTOK, WST, BST, DST>;
-  auto kern = moe_gemm_kernel<NMAT, NTOK, WST, BST, DST>;
+  using C = Cfg<NMAT, NTOK, KPS, WST, BST, DST>;
+  auto kern = moe_gemm_kernel<NMAT, NTOK, KPS, WST, BST, DST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   GemmArgs a;
@@ -446,9 +465,14 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 
 }  // namespace
 
-// gate/up: 6 x 32 KB weight stages, 4 x 6 KB activation stages, 4 partial buffers (384 columns)
-cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<2, kNTok, 6, 4, 4>(g, s); }
-// down: 12 x 16 KB weight stages, 4 x 6 KB activation stages, 8 partial buffers (384 columns)
-cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 12, 4, 8>(g, s); }
+// Weight stages are large on purpose: on GB300 a CTA's stream of bulk copies
+// completes at a roughly fixed number of copy groups per memory round trip, so
+// the bytes per stage set the bandwidth (a probe streaming into shared memory
+// reached 7.0 TB/s with 64 KB stages and 2.0 TB/s with 16 KB stages).
+// gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 x 6 KB activation stages,
+// 4 partial buffers (384 tensor-memory columns)
+cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<2, kNTok, 1, 6, 4, 4>(g, s); }
+// down: 3 stages of 4 K blocks = 64 KB, 4 x 6 KB activation stages, 8 partial buffers (384 columns)
+cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 4, 3, 4, 8>(g, s); }
 
 }  // namespace moe
