@@ -38,8 +38,8 @@ bool make_layout(const moe_dims* d, int64_t n, int32_t dff_sh, Layout* L) {
   if (!dims_ok(d) || n < 0 || dff_sh < 0 || dff_sh % 128 != 0) return false;
   const int64_t R = n * d->top_k;
   if (R >= (int64_t(1) << 31)) return false;
-  const int64_t max_tiles = R / kNTok + d->num_experts + 1;
-  const int64_t max_tiles_sh = n / kNTok + 2;
+  const int64_t max_tiles = R / kNTokSmall + d->num_experts + 1;  // bound for either tile width
+  const int64_t max_tiles_sh = n / kNTokSmall + 2;
   size_t off = 256;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -105,14 +105,14 @@ bool map_weights(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Split-format codes of `rows` sorted rows: [3 rows][K] e4m3, box 128 (K) x 3 kNTok
-// (three terms of kNTok rows), 128-byte swizzle; rows past the end read as zero.
-bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+// Split-format codes of `rows` sorted rows: [3 rows][K] e4m3, box 128 (K) x 3 ntok
+// (three terms of ntok rows), 128-byte swizzle; rows past the end read as zero.
+bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, int ntok) {
   EncodeFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {K, 3 * rows};
   const cuuint64_t strides[1] = {K};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(3 * kNTok)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(3 * ntok)};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -190,15 +190,17 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
         launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs, xs_inv, s));
     tr.after("gather_rows");
   }
-  MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, kNTok, tiles, n_tiles, s));
+  const int ntok = tile_tokens(R, d->num_experts);
+  MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, ntok, tiles, n_tiles, s));
   tr.after("build_tiles");
 
   CUtensorMap m_g, m_u, m_d, m_x, m_h;
-  if (!map_act(&m_x, xs, d->d, R) || !map_act(&m_h, h, d->d_ff, R)) return MOE_ERR_CUDA;
+  if (!map_act(&m_x, xs, d->d, R, ntok) || !map_act(&m_h, h, d->d_ff, R, ntok)) return MOE_ERR_CUDA;
   m_g = m_u = m_d = m_x;  // placeholders when the bank is tiled
   if (!map_bank(w, d->d, d->d_ff, d->num_experts, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
   const bool tiled = w->layout == MOE_LAYOUT_TILED;
   GemmLaunch g{};
+  g.ntok = ntok;
   g.w0 = &m_g;
   g.w1 = &m_u;
   g.w0_tiled = tiled ? w->w_gate : nullptr;
@@ -248,14 +250,16 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
   float* h_inv = at<float>(ws, L.h_sh_inv);
   TileDesc* tiles = at<TileDesc>(ws, L.tiles_sh);
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
-  MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), kNTok, tiles, n_tiles, s));
+  const int ntok = tile_tokens(n, 1);
+  MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), ntok, tiles, n_tiles, s));
   tr.after("shared_tiles");
   CUtensorMap m_g, m_u, m_d, m_x, m_h;
-  if (!map_act(&m_x, xs, d->d, n) || !map_act(&m_h, h, dff_sh, n)) return MOE_ERR_CUDA;
+  if (!map_act(&m_x, xs, d->d, n, ntok) || !map_act(&m_h, h, dff_sh, n, ntok)) return MOE_ERR_CUDA;
   m_g = m_u = m_d = m_x;
   if (!map_bank(w, d->d, dff_sh, 1, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
   const bool tiled = w->layout == MOE_LAYOUT_TILED;
   GemmLaunch g{};
+  g.ntok = ntok;
   g.w0 = &m_g;
   g.w1 = &m_u;
   g.w0_tiled = tiled ? w->w_gate : nullptr;

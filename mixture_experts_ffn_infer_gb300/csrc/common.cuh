@@ -50,8 +50,14 @@ struct TileDesc {
   int32_t pad;
 };
 
-// Token tile width of the grouped GEMMs (MMA N).
-constexpr int kNTok = 16;
+// Token tile widths of the grouped GEMMs (MMA N = 3 x tile: three e4m3 terms per
+// token).  Small tiles for decode-like batches (a few tokens per expert), large
+// tiles once experts see a few dozen tokens each.
+constexpr int kNTokSmall = 16;
+constexpr int kNTokLarge = 48;
+__host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
+  return rows >= 24 * experts ? kNTokLarge : kNTokSmall;
+}
 
 // ---------------------------------------------------------------- launchers
 // routing.cu
@@ -79,7 +85,8 @@ struct GemmLaunch {
   // weights: 3-D maps over [E][rows][K] e4m3, box 128 x 128 x 1, 128-byte swizzle
   const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
   const CUtensorMap* w1;        // up (gate/up pass only)
-  const CUtensorMap* act;       // 2-D map over the split activations [3 rows][K] e4m3, box 128 x 3 kNTok
+  const CUtensorMap* act;       // 2-D map over the split activations [3 rows][K] e4m3, box 128 x 3 ntok
+  int32_t ntok;                 // token tile width (kNTokSmall or kNTokLarge)
   const uint8_t* w0_tiled;      // tiled layout (moe_pack_weights): used instead of w0 / w1 when non-null
   const uint8_t* w1_tiled;
   const float* s0;              // scales [E][n_nb][num_kb]

@@ -339,38 +339,41 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       }
       // scales of the first K block; each iteration loads the next block's
       float s0n = __ldg(sc0), s1n = NMAT == 2 ? __ldg(sc1) : 0.f;
-      float sxn[NTOK];
-#pragma unroll
-      for (int j = 0; j < NTOK; ++j) sxn[j] = j < td.n_valid ? __ldg(a.act_inv + td.row_start + j) : 0.f;
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int sd = it % DST;
         const float s0v = s0n, s1v = s1n;
-        float sx[NTOK];  // 2^-s of each token's activation block
-#pragma unroll
-        for (int j = 0; j < NTOK; ++j) sx[j] = sxn[j];
+        // 2^-s of each token's activation block, [kb][row]; the next block's line is
+        // pulled into L1 now so the reads after the wait below hit
+        const float* inv = a.act_inv + static_cast<int64_t>(kb) * a.act_rows + td.row_start;
         if (kb + 1 < num_kb) {
           s0n = __ldg(sc0 + kb + 1);
           if (NMAT == 2) s1n = __ldg(sc1 + kb + 1);
-          const float* inv = a.act_inv + static_cast<int64_t>(kb + 1) * a.act_rows + td.row_start;
-#pragma unroll
-          for (int j = 0; j < NTOK; ++j) sxn[j] = j < td.n_valid ? __ldg(inv + j) : 0.f;
+          if (lane < (NTOK + 31) / 32 + 1 && td.row_start + lane * 32 < a.act_rows)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(inv + a.act_rows + lane * 32) : "memory");
         }
         ok = __all_sync(0xffffffffu, wait_bounded(dfull(sd), (it / DST) & 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const float sv = m == 0 ? s0v : s1v;
-          uint32_t p[NB];
+        for (int c = 0; c < NTOK / 16; ++c) {  // 16 tokens (48 tensor-memory columns) at a time
+          float sx[16];
 #pragma unroll
-          for (int c0 = 0; c0 < NB; c0 += 16)
-            tmem_ld16(tmem + lane_base + (sd * NMAT + m) * NB + c0, *reinterpret_cast<uint32_t(*)[16]>(&p[c0]));
-          tmem_ld_wait();
+          for (int j = 0; j < 16; ++j) sx[j] = 16 * c + j < td.n_valid ? __ldg(inv + 16 * c + j) : 0.f;
 #pragma unroll
-          for (int j = 0; j < NTOK; ++j) {
-            const float part = (__uint_as_float(p[3 * j]) + __uint_as_float(p[3 * j + 1])) +
-                               __uint_as_float(p[3 * j + 2]);
-            acc[m][j] = fmaf(sv * sx[j], part, acc[m][j]);
+          for (int m = 0; m < NMAT; ++m) {
+            const float sv = m == 0 ? s0v : s1v;
+            uint32_t p[48];
+#pragma unroll
+            for (int c0 = 0; c0 < 48; c0 += 16)
+              tmem_ld16(tmem + lane_base + (sd * NMAT + m) * NB + 48 * c + c0,
+                        *reinterpret_cast<uint32_t(*)[16]>(&p[c0]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float part = (__uint_as_float(p[3 * j]) + __uint_as_float(p[3 * j + 1])) +
+                                 __uint_as_float(p[3 * j + 2]);
+              acc[m][16 * c + j] = fmaf(sv * sx[j], part, acc[m][16 * c + j]);
+            }
           }
         }
         tc_fence_before();
@@ -385,7 +388,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         // The exchange goes through red[ui & 1] and an mbarrier of four arrivals, so a
         // warp can be one unit ahead of the others and every wait stays bounded.
         float* rb = red + (ui & 1) * 4 * NTOK;
-        float hv[NTOK];
+        float* hv = acc[0];  // h overwrites the gate accumulators
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) {
           const float g = acc[0][j];
@@ -469,10 +472,23 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 // completes at a roughly fixed number of copy groups per memory round trip, so
 // the bytes per stage set the bandwidth (a probe streaming into shared memory
 // reached 7.0 TB/s with 64 KB stages and 2.0 TB/s with 16 KB stages).
-// gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 x 6 KB activation stages,
-// 4 partial buffers (384 tensor-memory columns)
-cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<2, kNTok, 1, 6, 4, 4>(g, s); }
-// down: 3 stages of 4 K blocks = 64 KB, 4 x 6 KB activation stages, 8 partial buffers (384 columns)
-cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) { return launch_gemm<1, kNTok, 4, 3, 4, 8>(g, s); }
+// Decode-sized tiles (16 tokens, MMA N = 48):
+//   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 x 6 KB activation stages,
+//            4 partial buffers (384 tensor-memory columns)
+//   down:    3 stages of 4 K blocks = 64 KB, 4 x 6 KB activation stages, 8 partial buffers
+// Prefill-sized tiles (48 tokens, MMA N = 144: the weight tile in shared memory
+// serves three times the tokens per instruction):
+//   gate/up: 4 stages of 32 KB, 4 x 18 KB activation stages, 1 partial buffer (288 columns)
+//   down:    4 stages of 2 K blocks = 32 KB, 4 x 18 KB activation stages, 3 partial buffers
+cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
+  if (g.ntok == kNTokLarge) return launch_gemm<2, kNTokLarge, 1, 4, 4, 1>(g, s);
+  if (g.ntok == kNTokSmall) return launch_gemm<2, kNTokSmall, 1, 6, 4, 4>(g, s);
+  return cudaErrorInvalidValue;
+}
+cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) {
+  if (g.ntok == kNTokLarge) return launch_gemm<1, kNTokLarge, 2, 4, 4, 3>(g, s);
+  if (g.ntok == kNTokSmall) return launch_gemm<1, kNTokSmall, 4, 3, 4, 8>(g, s);
+  return cudaErrorInvalidValue;
+}
 
 }  // namespace moe
