@@ -147,6 +147,32 @@ def algorithmic(wl, ids_list, n_tokens):
             "step_bytes": step_bytes, "step_flops": flops}
 
 
+# ---------------------------------------------------------------------------- multi-rank host logic
+
+def rank_workload(wl, rank):
+    """Each rank draws its own batch (weak scaling): the seed moves by 1000 per rank; the
+    expert bank (bank_seed) is the same on every rank."""
+    from mixture_experts_ffn_infer_gb300 import synthetic as syn
+    return syn.Workload(**{**wl.__dict__, "seed": wl.seed + 1000 * rank,
+                           "bank_seed": syn.bank_seed_of(wl)})
+
+
+def max_over_ranks(value, world, device="cpu"):
+    """The slowest rank's time: all-reduce MAX (no-op on one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, steps, ms_total_max):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms_total_max / 1e3)
+
+
 # ---------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -163,7 +189,7 @@ def run_ours(args, rank, world, local_rank):
         wl = syn.Workload(**{**wl.__dict__, "num_experts": args.num_experts})
     mx.load_library()
     # each rank its own batch (seed offset by rank), the same resident weights
-    rank_wl = syn.Workload(**{**wl.__dict__, "seed": wl.seed + 1000 * rank})
+    rank_wl = rank_workload(wl, rank)
     x, ids, w, gain = syn.make_host_inputs(rank_wl)
     bank = syn.expert_bank(wl.num_experts, wl.d, wl.d_ff, syn.bank_seed_of(wl), dev)
     shared = syn.expert_bank(1, wl.d, wl.d_ff_shared, wl.seed + 1_000_003, dev) if wl.full_block else None
@@ -225,11 +251,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
 
     # per-kernel durations from the trace events of every timed step
     per_kernel = {}
@@ -272,10 +294,8 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    if not args.no_e2e:
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
     st = mx.moe_get_error(ws, stream)
     if st != mx.MOE_OK:
         raise RuntimeError(f"device error in the timed region: {mx.STATUS.get(st)}")
@@ -283,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
     alg = algorithmic(wl, [ids], n)
     ms_step = ms_total / args.steps
     tokens = n * world
-    value = tokens * args.steps / (ms_total / 1e3)
+    value = job_tokens_per_s(n, world, args.steps, ms_total)
     hbm, hbm_src = _hbm_peak()
     dominant = "gateup_swiglu"
     dom_ms = kern_ms.get(dominant)

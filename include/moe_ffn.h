@@ -213,6 +213,15 @@ moe_status moe_infer_static(const moe_dims *dims, int64_t n_tokens, const void *
                             const float *topk_weight, const moe_weights *weights, void *out, int32_t out_is_fp32,
                             cudaStream_t stream);
 
+/* Diagnostic of the failure path (no counterpart on the pages): launches one
+ * thread that waits on a barrier nothing will complete, through the same
+ * bounded wait every GEMM pipeline stage uses.  After about one second it gives
+ * up, records MOE_ERR_TIMEOUT in the workspace's error word and returns, so the
+ * GPU context stays usable; moe_get_error then reports MOE_ERR_TIMEOUT.  Lets a
+ * caller confirm that a stalled pipeline ends with a status, not a hang.
+ *   workspace: any buffer of at least 256 bytes, 256-byte aligned. */
+moe_status moe_check_bounded_wait(void *workspace, cudaStream_t stream);
+
 /* Synchronises `stream`, returns the first device-detected error recorded in
  * `workspace` since the last call (MOE_OK if none) and clears it. */
 moe_status moe_get_error(void *workspace, cudaStream_t stream);

@@ -79,6 +79,7 @@ _SIGS = {
                                          ctypes.c_void_p, ctypes.POINTER(moe_trace)]),
     "moe_infer_static": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 3
                          + [ctypes.POINTER(moe_weights), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "moe_check_bounded_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_get_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
 }
 
@@ -200,6 +201,11 @@ def moe_infer_static(dm, n_tokens, x, topk_ids, topk_weight, w: moe_weights, out
     st = load_library().moe_infer_static(ctypes.byref(dm), n_tokens, _ptr(x), _ptr(topk_ids), _ptr(topk_weight),
                                          ctypes.byref(w), _ptr(out), int(bool(out_is_fp32)), _stream(stream))
     _check(st, "moe_infer_static")
+
+
+def moe_check_bounded_wait(ws, stream=None):
+    st = load_library().moe_check_bounded_wait(_ptr(ws), _stream(stream))
+    _check(st, "moe_check_bounded_wait")
 
 
 def moe_get_error(ws, stream=None) -> int:

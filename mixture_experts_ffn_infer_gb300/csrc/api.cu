@@ -507,6 +507,12 @@ moe_status moe_infer_static(const moe_dims* dims, int64_t n, const void* x, cons
                    nullptr);
 }
 
+moe_status moe_check_bounded_wait(void* ws, cudaStream_t s) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (launch_bounded_wait_selftest(static_cast<uint32_t*>(ws), s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_get_error(void* ws, cudaStream_t s) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   uint32_t word = 0;

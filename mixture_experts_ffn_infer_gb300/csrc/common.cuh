@@ -66,6 +66,7 @@ cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32
                                  uint32_t* err, cudaStream_t s);
 cudaError_t launch_build_tiles(const int32_t* offsets, int32_t E, int32_t ntok, TileDesc* tiles,
                                int32_t* n_tiles, cudaStream_t s);
+cudaError_t launch_bounded_wait_selftest(uint32_t* err, cudaStream_t s);
 cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles, cudaStream_t s);
 
 // elementwise.cu

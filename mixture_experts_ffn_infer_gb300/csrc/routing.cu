@@ -158,7 +158,24 @@ __global__ void identity_tiles_kernel(int32_t rows, int32_t ntok, TileDesc* tile
   if (blockIdx.x == 0 && threadIdx.x == 0) *n_tiles = nt;
 }
 
+// One thread waits on a barrier that nothing completes, through the same bounded
+// wait the GEMM pipelines use; after the bound it raises DEV_ERR_TIMEOUT and exits.
+__global__ void bounded_wait_selftest_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0u;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  wait_bounded(smem_u32(&bar), 0, &abort_flag, err);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(uint32_t* err, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32_t E, int32_t* counts,
                                  int32_t* offsets, int32_t* sorted_pos, int32_t* inv_pos, int32_t validate,

@@ -37,34 +37,38 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _configure(L):
+    """Declare the C signatures on a loaded oracle library."""
+    i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+    L.oracle_e4m3_value.restype = dbl
+    L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    L.oracle_bf16_value.restype = dbl
+    L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    L.oracle_silu.restype = dbl
+    L.oracle_silu.argtypes = [dbl]
+    L.oracle_dequant.restype = dbl
+    L.oracle_dequant.argtypes = [vp, vp, i64, i64, i64, i64]
+    L.oracle_expert_forward.restype = None
+    L.oracle_expert_forward.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.oracle_rmsnorm.restype = None
+    L.oracle_rmsnorm.argtypes = [i64, i64, vp, vp, dbl, vp]
+    L.oracle_permute.restype = i64
+    L.oracle_permute.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+    L.oracle_moe_infer.restype = None
+    L.oracle_moe_infer.argtypes = [i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp, i64, vp, i32]
+    L.oracle_layer_forward.restype = None
+    L.oracle_layer_forward.argtypes = ([i64, i64, i64, i64, vp, vp, dbl, vp, vp] + [vp] * 6
+                                       + [vp] * 6 + [i64, vp, i64, vp, i32])
+    L.oracle_moe_infer_sorted.restype = None
+    L.oracle_moe_infer_sorted.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp]
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
-            i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
-            L.oracle_e4m3_value.restype = dbl
-            L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
-            L.oracle_bf16_value.restype = dbl
-            L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
-            L.oracle_silu.restype = dbl
-            L.oracle_silu.argtypes = [dbl]
-            L.oracle_dequant.restype = dbl
-            L.oracle_dequant.argtypes = [vp, vp, i64, i64, i64, i64]
-            L.oracle_expert_forward.restype = None
-            L.oracle_expert_forward.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
-            L.oracle_rmsnorm.restype = None
-            L.oracle_rmsnorm.argtypes = [i64, i64, vp, vp, dbl, vp]
-            L.oracle_permute.restype = i64
-            L.oracle_permute.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
-            L.oracle_moe_infer.restype = None
-            L.oracle_moe_infer.argtypes = [i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp, i64, vp, i32]
-            L.oracle_layer_forward.restype = None
-            L.oracle_layer_forward.argtypes = ([i64, i64, i64, i64, vp, vp, dbl, vp, vp] + [vp] * 6
-                                               + [vp] * 6 + [i64, vp, i64, vp, i32])
-            L.oracle_moe_infer_sorted.restype = None
-            L.oracle_moe_infer_sorted.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp]
-            _lib = L
+            _lib = _configure(ctypes.CDLL(build()))
     return _lib
 
 
