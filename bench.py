@@ -187,6 +187,8 @@ def run_ours(args, rank, world, local_rank):
     wl = syn.WORKLOADS[args.workload]
     if args.num_experts:
         wl = syn.Workload(**{**wl.__dict__, "num_experts": args.num_experts})
+    if args.n_tokens:
+        wl = syn.Workload(**{**wl.__dict__, "n_tokens": args.n_tokens})
     mx.load_library()
     # each rank its own batch (seed offset by rank), the same resident weights
     rank_wl = rank_workload(wl, rank)
@@ -468,6 +470,8 @@ def main():
     ap.add_argument("--ref-tokens-per-step", type=int, default=2)
     ap.add_argument("--num-experts", type=int, default=0,
                     help="override E (a smaller bank for profiling captures; routing redrawn over E)")
+    ap.add_argument("--n-tokens", type=int, default=0,
+                    help="override N (with --num-experts: a small case of the same rows per expert)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -119,6 +119,26 @@ bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, int nt
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Wide tiles: split-format codes as term planes [terms][rows][K] e4m3, box 128 (K)
+// x box_rows x terms, 128-byte swizzle; rows past the end read as zero.
+bool map_act_planar(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, int terms, int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {K, rows, static_cast<cuuint64_t>(terms)};
+  const cuuint64_t strides[2] = {K, K * rows};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(terms)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The split layout of `rows` sorted rows of width K, as the tile width chosen for
+// `rows` rows over `experts` experts reads it.
+SplitLayout rows_layout(int64_t rows, int64_t experts, int64_t K, int terms) {
+  return split_layout(tile_tokens(rows, experts) == kNTokWide, rows, K, terms);
+}
+
 int num_sms() {
   static std::atomic<int> cache[64];
   int dev = 0;
@@ -171,130 +191,119 @@ struct Tracer {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
-// The expert pass on an already-sorted routing plan: gather, gate/up, down.
-// `gather` selects the bf16 -> f16 row gather (moe_experts_forward / moe_infer);
-// the fused layer writes the sorted rows itself (RMSNorm scatter).
-moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float* topk_weight,
-                        const int32_t* offsets, const int32_t* sorted_pos, const moe_weights* w, void* rows,
-                        void* ws, const Layout& L, bool gather, cudaStream_t s, Tracer& tr) {
-  const int32_t R = static_cast<int32_t>(n * d->top_k);
-  uint8_t* xs = at<uint8_t>(ws, L.xs);
-  float* xs_inv = at<float>(ws, L.xs_inv);
-  uint8_t* h = at<uint8_t>(ws, L.h);
-  float* h_inv = at<float>(ws, L.h_inv);
-  TileDesc* tiles = at<TileDesc>(ws, L.tiles);
-  int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
-  uint32_t* err = at<uint32_t>(ws, L.err);
-  if (gather) {
-    MOE_CHECK_CUDA(
-        launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs, xs_inv, s));
-    tr.after("gather_rows");
+// Activation map of one GEMM pass: the 2-D map of 16-token tiles, or the planar
+// map of wide tiles (box of 128 rows x all terms).
+struct ActMaps {
+  CUtensorMap m16;
+  CUtensorMap box;
+  bool make(bool wide, const void* base, uint64_t K, uint64_t rows, int terms) {
+    if (!wide) return map_act(&m16, base, K, rows, kNTokSmall);
+    if (!map_act_planar(&box, base, K, rows, terms, kNTokWide)) return false;
+    m16 = box;
+    return true;
   }
-  const int ntok = tile_tokens(R, d->num_experts);
-  MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, ntok, tiles, n_tiles, s));
-  tr.after("build_tiles");
+  void bind(GemmLaunch& g) const {
+    g.act = &m16;
+    g.act_box = &box;
+  }
+};
 
-  CUtensorMap m_g, m_u, m_d, m_x, m_h;
-  if (!map_act(&m_x, xs, d->d, R, ntok) || !map_act(&m_h, h, d->d_ff, R, ntok)) return MOE_ERR_CUDA;
-  m_g = m_u = m_d = m_x;  // placeholders when the bank is tiled
-  if (!map_bank(w, d->d, d->d_ff, d->num_experts, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
+// Gate/up then down over `rows` sorted rows whose codes are already in xs (in
+// the layout rows_layout gives, x_terms terms), tiles cut at tile_tokens(rows,
+// experts) rows.  Down writes f16(topk_weight * o) to out[sorted_pos[row]]
+// (identity and weight 1 when those are null).
+moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t experts, int32_t rows, int x_terms,
+                     uint8_t* xs, float* xs_inv, uint8_t* h, float* h_inv, TileDesc* tiles, int32_t* n_tiles,
+                     const int32_t* sorted_pos, const float* topk_weight, void* out, uint32_t* err, cudaStream_t s,
+                     Tracer& tr, const char* label_gateup, const char* label_down) {
+  const int ntok = tile_tokens(rows, experts);
+  const bool wide = ntok == kNTokWide;
+  ActMaps mx, mh;
+  if (!mx.make(wide, xs, d, rows, x_terms) || !mh.make(wide, h, dff, rows, 3)) return MOE_ERR_CUDA;
+  CUtensorMap m_g, m_u, m_d;
+  m_g = m_u = m_d = mx.m16;  // placeholders when the bank is tiled
+  if (!map_bank(w, d, dff, experts, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
   const bool tiled = w->layout == MOE_LAYOUT_TILED;
   GemmLaunch g{};
   g.ntok = ntok;
+  g.terms = x_terms;
   g.w0 = &m_g;
   g.w1 = &m_u;
   g.w0_tiled = tiled ? w->w_gate : nullptr;
   g.w1_tiled = tiled ? w->w_up : nullptr;
-  g.act = &m_x;
+  mx.bind(g);
   g.s0 = w->s_gate;
   g.s1 = w->s_up;
   g.tiles = tiles;
   g.n_tiles = n_tiles;
-  g.n_nb = d->d_ff / 128;
-  g.num_kb = d->d / 128;
+  g.n_nb = static_cast<int32_t>(dff / 128);
+  g.num_kb = static_cast<int32_t>(d / 128);
   g.act_inv = xs_inv;
-  g.act_rows = R;
+  g.act_rows = rows;
   g.out = h;
   g.out_inv = h_inv;
   g.err = err;
   g.num_sms = num_sms();
   if (g.num_sms <= 0) return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gateup(g, s));
-  tr.after("gateup_swiglu");
+  tr.after(label_gateup);
 
   GemmLaunch q = g;
+  q.terms = 3;
   q.w0 = &m_d;
   q.w1 = &m_d;
   q.w0_tiled = q.w1_tiled = tiled ? w->w_down : nullptr;
-  q.act = &m_h;
+  mh.bind(q);
   q.s0 = w->s_down;
   q.s1 = w->s_down;
-  q.n_nb = d->d / 128;
-  q.num_kb = d->d_ff / 128;
+  q.n_nb = static_cast<int32_t>(d / 128);
+  q.num_kb = static_cast<int32_t>(dff / 128);
   q.act_inv = h_inv;
-  q.out = rows;
+  q.out = out;
   q.out_inv = nullptr;
   q.sorted_pos = sorted_pos;
   q.topk_weight = topk_weight;
   MOE_CHECK_CUDA(launch_down(q, s));
-  tr.after("down_scatter");
+  tr.after(label_down);
   return MOE_OK;
+}
+
+// The expert pass on an already-sorted routing plan: gather, gate/up, down.
+// `gather` selects the bf16 row gather (moe_experts_forward / moe_infer: two
+// terms carry a bf16 value); the fused layer writes the sorted rows itself
+// (RMSNorm scatter, three terms).
+moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float* topk_weight,
+                        const int32_t* offsets, const int32_t* sorted_pos, const moe_weights* w, void* rows,
+                        void* ws, const Layout& L, bool gather, cudaStream_t s, Tracer& tr) {
+  const int32_t R = static_cast<int32_t>(n * d->top_k);
+  uint8_t* xs = at<uint8_t>(ws, L.xs);
+  float* xs_inv = at<float>(ws, L.xs_inv);
+  TileDesc* tiles = at<TileDesc>(ws, L.tiles);
+  int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
+  const int x_terms = gather ? 2 : 3;
+  if (gather) {
+    MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs,
+                                      rows_layout(R, d->num_experts, d->d, x_terms), xs_inv, s));
+    tr.after("gather_rows");
+  }
+  MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
+  tr.after("build_tiles");
+  return run_gemms(w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
+                   at<float>(ws, L.h_inv), tiles, n_tiles, sorted_pos, topk_weight, rows, at<uint32_t>(ws, L.err), s,
+                   tr, "gateup_swiglu", "down_scatter");
 }
 
 // Shared expert on all n rows of xs_sh (identity order, weight 1) -> sh_out.
 moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32_t dff_sh, void* ws,
                        const Layout& L, cudaStream_t s, Tracer& tr) {
-  uint8_t* xs = at<uint8_t>(ws, L.xs_sh);
-  float* xs_inv = at<float>(ws, L.xs_sh_inv);
-  uint8_t* h = at<uint8_t>(ws, L.h_sh);
-  float* h_inv = at<float>(ws, L.h_sh_inv);
   TileDesc* tiles = at<TileDesc>(ws, L.tiles_sh);
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
-  const int ntok = tile_tokens(n, 1);
-  MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), ntok, tiles, n_tiles, s));
+  MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), tile_tokens(n, 1), tiles, n_tiles, s));
   tr.after("shared_tiles");
-  CUtensorMap m_g, m_u, m_d, m_x, m_h;
-  if (!map_act(&m_x, xs, d->d, n, ntok) || !map_act(&m_h, h, dff_sh, n, ntok)) return MOE_ERR_CUDA;
-  m_g = m_u = m_d = m_x;
-  if (!map_bank(w, d->d, dff_sh, 1, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
-  const bool tiled = w->layout == MOE_LAYOUT_TILED;
-  GemmLaunch g{};
-  g.ntok = ntok;
-  g.w0 = &m_g;
-  g.w1 = &m_u;
-  g.w0_tiled = tiled ? w->w_gate : nullptr;
-  g.w1_tiled = tiled ? w->w_up : nullptr;
-  g.act = &m_x;
-  g.s0 = w->s_gate;
-  g.s1 = w->s_up;
-  g.tiles = tiles;
-  g.n_tiles = n_tiles;
-  g.n_nb = dff_sh / 128;
-  g.num_kb = d->d / 128;
-  g.act_inv = xs_inv;
-  g.act_rows = static_cast<int32_t>(n);
-  g.out = h;
-  g.out_inv = h_inv;
-  g.err = at<uint32_t>(ws, L.err);
-  g.num_sms = num_sms();
-  if (g.num_sms <= 0) return MOE_ERR_CUDA;
-  MOE_CHECK_CUDA(launch_gateup(g, s));
-  tr.after("shared_gateup");
-  GemmLaunch q = g;
-  q.w0 = &m_d;
-  q.w1 = &m_d;
-  q.w0_tiled = q.w1_tiled = tiled ? w->w_down : nullptr;
-  q.act = &m_h;
-  q.s0 = w->s_down;
-  q.s1 = w->s_down;
-  q.n_nb = d->d / 128;
-  q.num_kb = dff_sh / 128;
-  q.act_inv = h_inv;
-  q.out = at<uint16_t>(ws, L.sh_out);
-  q.out_inv = nullptr;
-  MOE_CHECK_CUDA(launch_down(q, s));
-  tr.after("shared_down");
-  return MOE_OK;
+  return run_gemms(w, d->d, dff_sh, 1, static_cast<int32_t>(n), 3, at<uint8_t>(ws, L.xs_sh),
+                   at<float>(ws, L.xs_sh_inv), at<uint8_t>(ws, L.h_sh), at<float>(ws, L.h_sh_inv), tiles, n_tiles,
+                   nullptr, nullptr, at<uint16_t>(ws, L.sh_out), at<uint32_t>(ws, L.err), s, tr, "shared_gateup",
+                   "shared_down");
 }
 
 }  // namespace
@@ -472,10 +481,12 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
   MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
                                       offsets, sp, ip, 0, err, s));
   tr.after("route_permute");
-  MOE_CHECK_CUDA(launch_rmsnorm_scatter(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain),
-                                        eps, static_cast<int32_t>(n), dims->d, dims->top_k, ip, at<uint8_t>(ws, L.xs),
-                                        at<float>(ws, L.xs_inv), shared ? at<uint8_t>(ws, L.xs_sh) : nullptr,
-                                        shared ? at<float>(ws, L.xs_sh_inv) : nullptr, s));
+  const int64_t R = n * dims->top_k;
+  MOE_CHECK_CUDA(launch_rmsnorm_scatter(
+      static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain), eps, static_cast<int32_t>(n), dims->d,
+      dims->top_k, ip, at<uint8_t>(ws, L.xs), rows_layout(R, dims->num_experts, dims->d, 3), at<float>(ws, L.xs_inv),
+      shared ? at<uint8_t>(ws, L.xs_sh) : nullptr, rows_layout(n, 1, dims->d, 3),
+      shared ? at<float>(ws, L.xs_sh_inv) : nullptr, s));
   tr.after("rmsnorm_scatter");
   void* rows = at<void>(ws, L.rows);
   moe_status st = experts_pass(dims, n, nullptr, topk_weight, offsets, sp, routed, rows, ws, L, false, s, tr);

@@ -50,13 +50,29 @@ struct TileDesc {
   int32_t pad;
 };
 
-// Token tile widths of the grouped GEMMs (MMA N = 3 x tile: three e4m3 terms per
-// token).  Small tiles for decode-like batches (a few tokens per expert), large
-// tiles once experts see a few dozen tokens each.
+// Token tile widths of the grouped GEMMs.  Decode-like batches (a few rows per
+// expert) use 16-token tiles whose three activation terms sit side by side on
+// the MMA's N axis (N = 48); from 24 rows per expert on, tiles of up to 128
+// tokens with the terms stacked along K (N = tile rows rounded up to 16).
 constexpr int kNTokSmall = 16;
-constexpr int kNTokLarge = 48;
+constexpr int kNTokWide = 128;
 __host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
-  return rows >= 24 * experts ? kNTokLarge : kNTokSmall;
+  return rows >= 24 * experts ? kNTokWide : kNTokSmall;
+}
+
+// Where the split-format codes of a sorted row live (split3.cuh): term t of
+// row i starts at base + i * row_stride + t * term_stride bytes.
+//   16-token tiles: rows interleaved with their terms, [rows][3][K]
+//                   (row_stride 3K, term_stride K, 3 terms)
+//   wide tiles:     one plane per term, [terms][rows][K]
+//                   (row_stride K, term_stride rows * K, 2 or 3 terms)
+struct SplitLayout {
+  int64_t row_stride;
+  int64_t term_stride;
+  int32_t terms;
+};
+inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms) {
+  return wide ? SplitLayout{K, rows * K, terms} : SplitLayout{3 * K, K, 3};
 }
 
 // ---------------------------------------------------------------- launchers
@@ -72,10 +88,11 @@ cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, i
 // elementwise.cu
 // Sorted activation rows in the split format: codes [3 R][d] e4m3 + exponents [d/128][R].
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k,
-                               int32_t d, uint8_t* xs, float* xs_inv, cudaStream_t s);
+                               int32_t d, uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s);
 cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_bf16, float eps, int32_t n,
-                                   int32_t d, int32_t k, const int32_t* inv_pos, uint8_t* xs, float* xs_inv,
-                                   uint8_t* xs_shared, float* xs_shared_inv, cudaStream_t s);
+                                   int32_t d, int32_t k, const int32_t* inv_pos, uint8_t* xs, SplitLayout lay,
+                                   float* xs_inv, uint8_t* xs_shared, SplitLayout lay_shared, float* xs_shared_inv,
+                                   cudaStream_t s);
 cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_experts, int32_t rows, int32_t cols,
                               cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* rows_f16, const uint16_t* shared_f16, const uint16_t* resid_bf16,
@@ -86,8 +103,10 @@ struct GemmLaunch {
   // weights: 3-D maps over [E][rows][K] e4m3, box 128 x 128 x 1, 128-byte swizzle
   const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
   const CUtensorMap* w1;        // up (gate/up pass only)
-  const CUtensorMap* act;       // 2-D map over the split activations [3 rows][K] e4m3, box 128 x 3 ntok
-  int32_t ntok;                 // token tile width (kNTokSmall or kNTokLarge)
+  const CUtensorMap* act;       // 16-token tiles: 2-D map over [3 rows][K] e4m3, box 128 x 48
+  const CUtensorMap* act_box;   // wide tiles: 3-D map over [terms][rows][K], box 128 x 128 rows x terms
+  int32_t ntok;                 // token tile width (kNTokSmall or kNTokWide)
+  int32_t terms;                // wide tiles: activation terms (2 or 3)
   const uint8_t* w0_tiled;      // tiled layout (moe_pack_weights): used instead of w0 / w1 when non-null
   const uint8_t* w1_tiled;
   const float* s0;              // scales [E][n_nb][num_kb]
@@ -98,7 +117,7 @@ struct GemmLaunch {
   int32_t num_kb;               // K / 128
   const float* act_inv;         // [num_kb][act_rows] 2^-s of each activation block
   int32_t act_rows;             // rows of the sorted activation matrix
-  void* out;                    // gate/up: h terms [3 act_rows][n_nb*128] e4m3; down: rows [.][n_nb*128] f16
+  void* out;                    // gate/up: h codes (layout of the next pass); down: rows [.][n_nb*128] f16
   float* out_inv;               // gate/up: [n_nb][act_rows] 2^-s of each h block
   const int32_t* sorted_pos;    // down: flat position of each sorted row (NULL = identity)
   const float* topk_weight;     // down: flat router weights (NULL = 1)
@@ -107,5 +126,8 @@ struct GemmLaunch {
 };
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s);
+// moe_gemm_wide.cu (the two above forward wide tiles here)
+cudaError_t launch_gateup_wide(const GemmLaunch& g, cudaStream_t s);
+cudaError_t launch_down_wide(const GemmLaunch& g, cudaStream_t s);
 
 }  // namespace moe

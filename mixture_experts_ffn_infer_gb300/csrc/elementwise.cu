@@ -28,10 +28,6 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -45,7 +41,7 @@ constexpr int kRowThreads = 256;  // eight warps per row, one 128-column block p
 __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                                   const int32_t* __restrict__ sorted_pos, int32_t R,
                                                                   int32_t k, int32_t d, uint8_t* __restrict__ xs,
-                                                                  float* __restrict__ xs_inv) {
+                                                                  SplitLayout lay, float* __restrict__ xs_inv) {
   const int64_t i = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = sorted_pos[i];
@@ -61,14 +57,14 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
     }
     uint32_t t1, t2, t3;
     const float inv = warp_split_block(v, t1, t2, t3);
-    warp_store_block(xs, d, xs_inv, R, i, kb, t1, t2, t3, inv, lane);
+    warp_store_block(xs, lay, xs_inv, R, i, kb, t1, t2, t3, inv, lane);
   }
 }
 
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
     const uint16_t* __restrict__ h, const uint16_t* __restrict__ gain, float eps, int32_t n, int32_t d, int32_t k,
-    const int32_t* __restrict__ inv_pos, uint8_t* __restrict__ xs, float* __restrict__ xs_inv,
-    uint8_t* __restrict__ xs_shared, float* __restrict__ xs_shared_inv) {
+    const int32_t* __restrict__ inv_pos, uint8_t* __restrict__ xs, SplitLayout lay, float* __restrict__ xs_inv,
+    uint8_t* __restrict__ xs_shared, SplitLayout lay_shared, float* __restrict__ xs_shared_inv) {
   __shared__ float red[kRowThreads / 32];
   __shared__ float s_inv;
   const int64_t t = blockIdx.x;
@@ -115,8 +111,8 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
     v[3] = bf16_hi(g.y) * (bf16_hi(w.y) * inv_rms);
     uint32_t t1, t2, t3;
     const float inv = warp_split_block(v, t1, t2, t3);
-    for (int q = 0; q < ndst; ++q) warp_store_block(xs, d, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
-    if (xs_shared) warp_store_block(xs_shared, d, xs_shared_inv, n, t, kb, t1, t2, t3, inv, lane);
+    for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
+    if (xs_shared) warp_store_block(xs_shared, lay_shared, xs_shared_inv, n, t, kb, t1, t2, t3, inv, lane);
   }
 }
 
@@ -201,18 +197,18 @@ cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_expe
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k, int32_t d,
-                               uint8_t* xs, float* xs_inv, cudaStream_t s) {
+                               uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
-  gather_rows_kernel<<<R, kRowThreads, 0, s>>>(x_bf16, sorted_pos, R, k, d, xs, xs_inv);
+  gather_rows_kernel<<<R, kRowThreads, 0, s>>>(x_bf16, sorted_pos, R, k, d, xs, lay, xs_inv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_bf16, float eps, int32_t n, int32_t d,
-                                   int32_t k, const int32_t* inv_pos, uint8_t* xs, float* xs_inv, uint8_t* xs_shared,
-                                   float* xs_shared_inv, cudaStream_t s) {
+                                   int32_t k, const int32_t* inv_pos, uint8_t* xs, SplitLayout lay, float* xs_inv,
+                                   uint8_t* xs_shared, SplitLayout lay_shared, float* xs_shared_inv, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  rmsnorm_scatter_kernel<<<n, kRowThreads, 0, s>>>(h_bf16, gain_bf16, eps, n, d, k, inv_pos, xs, xs_inv, xs_shared,
-                                                   xs_shared_inv);
+  rmsnorm_scatter_kernel<<<n, kRowThreads, 0, s>>>(h_bf16, gain_bf16, eps, n, d, k, inv_pos, xs, lay, xs_inv,
+                                                   xs_shared, lay_shared, xs_shared_inv);
   return cudaGetLastError();
 }
 

@@ -476,17 +476,14 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 //   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 x 6 KB activation stages,
 //            4 partial buffers (384 tensor-memory columns)
 //   down:    3 stages of 4 K blocks = 64 KB, 4 x 6 KB activation stages, 8 partial buffers
-// Prefill-sized tiles (48 tokens, MMA N = 144: the weight tile in shared memory
-// serves three times the tokens per instruction):
-//   gate/up: 4 stages of 32 KB, 4 x 18 KB activation stages, 1 partial buffer (288 columns)
-//   down:    4 stages of 2 K blocks = 32 KB, 4 x 18 KB activation stages, 3 partial buffers
+// Wide tiles (up to 128 tokens) go to moe_gemm_wide.cu.
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
-  if (g.ntok == kNTokLarge) return launch_gemm<2, kNTokLarge, 1, 4, 4, 1>(g, s);
+  if (g.ntok == kNTokWide) return launch_gateup_wide(g, s);
   if (g.ntok == kNTokSmall) return launch_gemm<2, kNTokSmall, 1, 6, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) {
-  if (g.ntok == kNTokLarge) return launch_gemm<1, kNTokLarge, 2, 4, 4, 3>(g, s);
+  if (g.ntok == kNTokWide) return launch_down_wide(g, s);
   if (g.ntok == kNTokSmall) return launch_gemm<1, kNTokSmall, 4, 3, 4, 8>(g, s);
   return cudaErrorInvalidValue;
 }

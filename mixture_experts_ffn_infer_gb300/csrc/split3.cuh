@@ -16,6 +16,8 @@
 
 #include <cstdint>
 
+#include "common.cuh"
+
 namespace moe {
 
 __device__ __forceinline__ float e4m3_to_float(uint8_t v) {
@@ -73,16 +75,16 @@ __device__ __forceinline__ float warp_split_block(const float (&v)[4], uint32_t&
   return ldexpf(1.0f, -s);
 }
 
-// Store a block converted by warp_split_block for sorted row `row`: the terms
-// go to rows 3 row + t of the [3 rows][ld] code matrix at column block kb, the
-// exponent to inv[kb * n_rows + row].
-__device__ __forceinline__ void warp_store_block(uint8_t* terms, int64_t ld, float* inv, int64_t n_rows, int64_t row,
-                                                 int kb, uint32_t t1, uint32_t t2, uint32_t t3, float inv_s,
-                                                 int lane) {
-  uint8_t* base = terms + 3 * row * ld + static_cast<int64_t>(kb) * 128;
+// Store a block converted by warp_split_block for sorted row `row` at column
+// block kb: the codes go where `lay` puts them (the third term only when the
+// layout keeps three), the exponent to inv[kb * n_rows + row].
+__device__ __forceinline__ void warp_store_block(uint8_t* codes, SplitLayout lay, float* inv, int64_t n_rows,
+                                                 int64_t row, int kb, uint32_t t1, uint32_t t2, uint32_t t3,
+                                                 float inv_s, int lane) {
+  uint8_t* base = codes + row * lay.row_stride + static_cast<int64_t>(kb) * 128;
   reinterpret_cast<uint32_t*>(base)[lane] = t1;
-  reinterpret_cast<uint32_t*>(base + ld)[lane] = t2;
-  reinterpret_cast<uint32_t*>(base + 2 * ld)[lane] = t3;
+  reinterpret_cast<uint32_t*>(base + lay.term_stride)[lane] = t2;
+  if (lay.terms > 2) reinterpret_cast<uint32_t*>(base + 2 * lay.term_stride)[lane] = t3;
   if (lane == 0) inv[static_cast<int64_t>(kb) * n_rows + row] = inv_s;
 }
 

@@ -43,6 +43,8 @@ def test_tiny_infer_bf16_and_fp32_outputs():
     (200, 512, 128, 64, 6, 3),     # many experts, most with few rows
     (300, 384, 256, 3, 1, 4),      # k = 1, a hundred rows per expert (several token tiles)
     (64, 128, 128, 1, 1, 5),       # single expert
+    (600, 256, 256, 2, 1, 6),      # 300 rows per expert: tiles of 128, 128 and 44 rows
+    (150, 1152, 256, 4, 2, 8),     # nine 128-row blocks of down: the last pair has one block
 ])
 def test_small_shapes_infer(n, d, dff, E, k, seed):
     wl = syn.Workload("s", n, d, dff, E, k, seed=seed)
@@ -106,6 +108,16 @@ def test_layer_forward_small_with_shared_expert():
     y2 = mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, None)
     ref2 = oracle.layer_forward(c.inp.x, c.inp.gain, c.inp.eps, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
     _assert_ok(y2, ref2)
+
+
+def test_layer_forward_wide_tiles_three_terms():
+    # 200 routed rows per expert and 300 shared rows: tiles of 128 rows, the
+    # normalised features in three terms
+    wl = syn.Workload("blkw", 300, 384, 256, 3, 2, full_block=True, d_ff_shared=256, seed=11)
+    c = cases.workload(wl)
+    ref = oracle.layer_forward(c.inp.x, c.inp.gain, c.inp.eps, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank,
+                               c.inp.shared)
+    _assert_ok(mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, c.shared), ref)
 
 
 def test_deterministic_and_zero_tokens():
