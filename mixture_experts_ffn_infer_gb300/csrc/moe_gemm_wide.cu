@@ -152,13 +152,23 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&p)[64]) {
   for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&p[16 * c]));
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and division; for
+// g < -87 the denominator overflows and the result is 0 (the exact value is
+// below 1e-36).
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// Four values -> one word of e4m3 codes per term, v * 2^s split as in split3.
-__device__ __forceinline__ void split_word(float v0, float v1, float v2, float v3, int s, uint32_t& w1,
-                                           uint32_t& w2, uint32_t& w3) {
-  const float v[4] = {v0, v1, v2, v3};
-  split3x4(v, s, w1, w2, w3);
+// 16 values of one token, scaled by f1 * f2 = 2^s -> 16 codes of each term.
+__device__ __forceinline__ void split16(const float* v, float f1, float f2, uint32_t (&w1)[4], uint32_t (&w2)[4],
+                                        uint32_t (&w3)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a1, a2, a3, b1, b2, b3;
+    split3_pair(make_float2(v[4 * i] * f1 * f2, v[4 * i + 1] * f1 * f2), a1, a2, a3);
+    split3_pair(make_float2(v[4 * i + 2] * f1 * f2, v[4 * i + 3] * f1 * f2), b1, b2, b3);
+    w1[i] = a1 | (b1 << 16);
+    w2[i] = a2 | (b2 << 16);
+    w3[i] = a3 | (b3 << 16);
+  }
 }
 
 template <bool GATEUP, int TX, int WST, int AST>
@@ -408,9 +418,9 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
         float m = 0.f;
 #pragma unroll
         for (int j = 0; j < kHalfF; ++j) {
-          acc0[j] = silu(acc0[j]) * acc1[j];
+          acc0[j] = silu_fast(acc0[j]) * acc1[j];
           m = fmaxf(m, fabsf(acc0[j]));
-          overflow |= !isfinite(acc0[j]);
+          overflow |= !(fabsf(acc0[j]) <= 3.0e38f);
         }
         overflow &= valid;
         float* rb = red + (ui & 1) * 2 * kTileMax;
@@ -421,49 +431,40 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
         if (!ok) break;
         if (valid) {
           const int sexp = split_exponent(fmaxf(m, rb[(hf ^ 1) * kTileMax + tok]));
+          const float f1 = pow2i(sexp >> 1), f2 = pow2i(sexp - (sexp >> 1));  // both factors stay normal
           const int64_t ld = static_cast<int64_t>(n_nb) * 128;
           uint8_t* hp = static_cast<uint8_t*>(a.out) + row * ld + un.nb0 * 128 + hf * kHalfF;
 #pragma unroll
-          for (int v = 0; v < kHalfF / 16; ++v) {
-            uint4 t1, t2, t3;
-            split_word(acc0[16 * v + 0], acc0[16 * v + 1], acc0[16 * v + 2], acc0[16 * v + 3], sexp, t1.x, t2.x, t3.x);
-            split_word(acc0[16 * v + 4], acc0[16 * v + 5], acc0[16 * v + 6], acc0[16 * v + 7], sexp, t1.y, t2.y, t3.y);
-            split_word(acc0[16 * v + 8], acc0[16 * v + 9], acc0[16 * v + 10], acc0[16 * v + 11], sexp, t1.z, t2.z,
-                       t3.z);
-            split_word(acc0[16 * v + 12], acc0[16 * v + 13], acc0[16 * v + 14], acc0[16 * v + 15], sexp, t1.w, t2.w,
-                       t3.w);
-            reinterpret_cast<uint4*>(hp)[v] = t1;
-            reinterpret_cast<uint4*>(hp + a.out_plane)[v] = t2;
-            reinterpret_cast<uint4*>(hp + 2 * a.out_plane)[v] = t3;
+          for (int v = 0; v < kHalfF / 32; ++v) {
+            uint32_t t1[8], t2[8], t3[8];
+            split16(acc0 + 32 * v, f1, f2, *reinterpret_cast<uint32_t(*)[4]>(&t1[0]),
+                    *reinterpret_cast<uint32_t(*)[4]>(&t2[0]), *reinterpret_cast<uint32_t(*)[4]>(&t3[0]));
+            split16(acc0 + 32 * v + 16, f1, f2, *reinterpret_cast<uint32_t(*)[4]>(&t1[4]),
+                    *reinterpret_cast<uint32_t(*)[4]>(&t2[4]), *reinterpret_cast<uint32_t(*)[4]>(&t3[4]));
+            stg256(hp + 32 * v, t1);
+            stg256(hp + a.out_plane + 32 * v, t2);
+            stg256(hp + 2 * a.out_plane + 32 * v, t3);
           }
-          if (hf == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = ldexpf(1.0f, -sexp);
+          if (hf == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = pow2i(-(sexp >> 1)) *
+                                                                                      pow2i((sexp >> 1) - sexp);
         }
       } else if (valid) {
         uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(dst) * n_nb * 128 + hf * kHalfF;
 #pragma unroll
-        for (int v = 0; v < kHalfF / 8; ++v) {
-          uint32_t w[4];
+        for (int m = 0; m < 2; ++m) {
+          if (m == 1 && !un.has1) break;
+          const float* src = m == 0 ? acc0 : acc1;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float x0 = acc0[8 * v + 2 * i] * wg, x1 = acc0[8 * v + 2 * i + 1] * wg;
-            overflow |= !(fabsf(x0) < 65520.f) || !(fabsf(x1) < 65520.f);
-            const __half2 h2 = __floats2half2_rn(x0, x1);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          reinterpret_cast<uint4*>(o + un.nb0 * 128)[v] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        if (un.has1) {
+          for (int v = 0; v < kHalfF / 16; ++v) {
+            uint32_t w[8];
 #pragma unroll
-          for (int v = 0; v < kHalfF / 8; ++v) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float x0 = acc1[8 * v + 2 * i] * wg, x1 = acc1[8 * v + 2 * i + 1] * wg;
-              overflow |= !(fabsf(x0) < 65520.f) || !(fabsf(x1) < 65520.f);
+            for (int i = 0; i < 8; ++i) {
+              const float x0 = src[16 * v + 2 * i] * wg, x1 = src[16 * v + 2 * i + 1] * wg;
+              overflow |= !(fabsf(x0) < 65520.f) || !(fabsf(x1) < 65520.f);  // f16 rounds these to inf
               const __half2 h2 = __floats2half2_rn(x0, x1);
               w[i] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            reinterpret_cast<uint4*>(o + un.nb1 * 128)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            stg256(o + (m == 0 ? un.nb0 : un.nb1) * 128 + 16 * v, w);
           }
         }
       }
