@@ -24,16 +24,23 @@
  *     sum each token's k outputs weighted by topk_weight.  The page's prose:
  *     each token's output is the router-weighted sum of its selected experts
  *     plus the shared expert applied to every token.
- *   - "Input features" page, RMSNorm excerpt: y = gain * h / sqrt(mean(h^2) + eps);
- *     decoder block: hidden = residual + mlp(post_attention_norm(residual)).
+ *   - "Input features" page, RMSNorm excerpt: the row is promoted to float32,
+ *     variance = mean(h^2), h * rsqrt(variance + eps), the result is cast back
+ *     to the input dtype (bf16) and multiplied by the bf16 gain (a bf16
+ *     product); decoder block: hidden = residual + mlp(post_attention_norm(residual)).
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *   - sort order of equal expert ids: ascending flat index t*k + j (stable);
  *   - counting: a histogram that adds (a token naming one expert twice is
  *     counted twice);
  *   - the activation is SiLU, silu(a) = a / (1 + exp(-a));
- *   - no intermediate rounding to bf16 anywhere (the exact function; any
- *     rounding an implementation does is covered by the parity tolerance);
+ *   - RMSNorm follows the excerpt's own precision: float32 arithmetic and the
+ *     two bf16 roundings it writes; the variance is the exact mean of squares
+ *     rounded once to float32 (a float32 sum in some order differs from it
+ *     only in the last bits);
+ *   - everything after RMSNorm has no intermediate rounding (the exact
+ *     function; the roundings an implementation does are covered by the
+ *     parity tolerance);
  *   - summation order: ((sum over j ascending of w_j * E_j(x)) + shared(x)) + residual.
  */
 #include <math.h>
@@ -168,7 +175,19 @@ void oracle_expert_forward(int64_t n_rows, int64_t d, int64_t dff, const double 
 /* RMSNorm                                                                   */
 /* ------------------------------------------------------------------------- */
 
-/* xn = gain * h / sqrt(mean(h^2) + eps), one row. */
+/* Nearest bfloat16 to a finite binary32 value, ties to even: the upper half of
+ * the pattern after adding just under half of the dropped part, plus one more
+ * when the kept part is odd. */
+static float bf16_round(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* xn = bf16(gain * bf16(h * rsqrt(mean(h^2) + eps))), float32 arithmetic, one row. */
 static void rmsnorm_row(int64_t d, const uint16_t *h_bf16, const uint16_t *gain_bf16, double eps, double *xn)
 {
     double ss = 0.0;
@@ -176,9 +195,12 @@ static void rmsnorm_row(int64_t d, const uint16_t *h_bf16, const uint16_t *gain_
         double v = oracle_bf16_value(h_bf16[c]);
         ss += v * v;
     }
-    double inv = 1.0 / sqrt(ss / (double)d + eps);
-    for (int64_t c = 0; c < d; ++c)
-        xn[c] = oracle_bf16_value(gain_bf16[c]) * (oracle_bf16_value(h_bf16[c]) * inv);
+    float variance = (float)(ss / (double)d);
+    float inv = 1.0f / sqrtf(variance + (float)eps);
+    for (int64_t c = 0; c < d; ++c) {
+        float normed = bf16_round((float)oracle_bf16_value(h_bf16[c]) * inv);
+        xn[c] = (double)bf16_round((float)oracle_bf16_value(gain_bf16[c]) * normed);
+    }
 }
 
 void oracle_rmsnorm(int64_t n, int64_t d, const uint16_t *h_bf16, const uint16_t *gain_bf16, double eps, double *xn)

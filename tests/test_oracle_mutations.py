@@ -26,7 +26,9 @@ MUTATIONS = {
     "input index reversed": ("a += wq(&ex->gate, f, c) * x[c];", "a += wq(&ex->gate, f, c) * x[d - 1 - c];"),
     "router weight dropped": ("acc[c] += wt * o[c];", "acc[c] += o[c];"),
     "e4m3 bias off by one": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
-    "rmsnorm eps dropped": ("sqrt(ss / (double)d + eps)", "sqrt(ss / (double)d)"),
+    "rmsnorm eps dropped": ("sqrtf(variance + (float)eps)", "sqrtf(variance)"),
+    "rmsnorm cast to bf16 dropped": ("float normed = bf16_round((float)oracle_bf16_value(h_bf16[c]) * inv);",
+                                     "float normed = (float)oracle_bf16_value(h_bf16[c]) * inv;"),
     "sort ties reversed": ("    for (int64_t p = 0; p < R; ++p) {\n        int32_t e = ids[p];",
                            "    for (int64_t p = R - 1; p >= 0; --p) {\n        int32_t e = ids[p];"),
     "residual dropped": ("acc[c] += oracle_bf16_value(jb->resid[t * d + c]);", "(void)0;"),

@@ -161,17 +161,28 @@ def _bf16_bits(t):
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def _bf16_round(a):
+    """Nearest bf16 of float32 values, through torch's own conversion."""
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).double().numpy()
+
+
 def test_rmsnorm_constant_rows_closed_form():
+    # A constant row c has mean square c^2: with eps = 0 the normalised row is
+    # sign(c) exactly, and the output is bf16(gain * sign(c)) = +-gain.
     d = 512
-    for cval in (0.5, -3.0, 1e-3):
-        h = torch.full((1, d), cval)
-        gain = torch.linspace(0.5, 1.5, d)
-        hb, gb = _bf16_bits(h), _bf16_bits(gain)
-        cb = float(torch.tensor(cval).to(torch.bfloat16))
-        eps = 1e-6
-        ours = oracle.rmsnorm(hb, gb, eps)
-        ref = gain.to(torch.bfloat16).double().numpy() * cb / math.sqrt(cb * cb + eps)
-        assert np.allclose(ours[0], ref, rtol=1e-14)
+    gain = torch.linspace(0.5, 1.5, d)
+    gb = _bf16_bits(gain)
+    g = gain.to(torch.bfloat16).double().numpy()
+    for cval in (0.5, -3.0, 1e-3, 96.0):
+        hb = _bf16_bits(torch.full((1, d), cval))
+        assert np.array_equal(oracle.rmsnorm(hb, gb, 0.0)[0], np.sign(cval) * g)
+    # eps enters as mean(h^2) + eps: 0.5 / sqrt(0.25 + 0.75) = 0.5 exactly
+    ones = _bf16_bits(torch.ones(d))
+    y = oracle.rmsnorm(_bf16_bits(torch.full((1, d), 0.5)), ones, 0.75)
+    assert np.array_equal(y, np.full((1, d), 0.5))
+    # and 3 / sqrt(9 + 7) = 0.75
+    y = oracle.rmsnorm(_bf16_bits(torch.full((1, d), 3.0)), ones, 7.0)
+    assert np.array_equal(y, np.full((1, d), 0.75))
 
 
 def test_rmsnorm_invariants():
@@ -179,19 +190,21 @@ def test_rmsnorm_invariants():
     h = torch.randn(4, d, generator=torch.Generator().manual_seed(1))
     ones = torch.ones(d)
     xn = oracle.rmsnorm(_bf16_bits(h), _bf16_bits(ones), 0.0)
-    # unit gain, eps = 0: every output row has mean square exactly 1
-    assert np.allclose((xn ** 2).mean(axis=1), 1.0, rtol=1e-13)
+    # the output is a bf16 tensor, as the excerpt's cast makes it
+    assert np.array_equal(xn, _bf16_round(xn))
+    # unit gain, eps = 0: every output row has mean square 1 up to the bf16 rounding
+    assert np.allclose((xn ** 2).mean(axis=1), 1.0, rtol=2e-3)
+    # the unrounded normalised row is h / rms(h); the output is its nearest bf16
+    hd = h.to(torch.bfloat16).double().numpy()
+    exact = hd / np.sqrt((hd ** 2).mean(axis=1, keepdims=True))
+    assert np.max(np.abs(xn - exact) / np.abs(exact)) <= 2.0 ** -8 * (1 + 1e-6)
     # scale invariance (power-of-two scale keeps the bf16 input exact)
     xn2 = oracle.rmsnorm(_bf16_bits(h * 8.0), _bf16_bits(ones), 0.0)
-    assert np.allclose(xn, xn2, rtol=1e-14)
-    # eps enters as mean(h^2) + eps
-    hb = torch.full((1, d), 0.5)
-    y = oracle.rmsnorm(_bf16_bits(hb), _bf16_bits(ones), 0.75)
-    assert np.allclose(y, 0.5 / math.sqrt(0.25 + 0.75), rtol=1e-15)
-    # gain multiplies feature-wise
+    assert np.array_equal(xn, xn2)
+    # the gain multiplies the bf16 normalised row feature-wise, then rounds once more
     gain = torch.linspace(-2, 2, d).to(torch.bfloat16)
     yg = oracle.rmsnorm(_bf16_bits(h), _bf16_bits(gain), 0.0)
-    assert np.allclose(yg, xn * gain.double().numpy()[None, :], rtol=1e-14, atol=1e-300)
+    assert np.array_equal(yg, _bf16_round(xn * gain.double().numpy()[None, :]))
 
 
 # ---------------------------------------------------------------- routing plan
@@ -335,9 +348,13 @@ def test_layer_forward_matches_fp64_restatement():
     inp = syn.make_inputs(wl)
     y = oracle.layer_forward(inp.x, inp.gain, inp.eps, inp.topk_ids, inp.topk_weight, inp.bank, inp.shared)
     h = inp.x.double()
-    ms = (h * h).mean(dim=1, keepdim=True)
-    xn = inp.gain.double()[None, :] * (h / torch.sqrt(ms + inp.eps))
-    # routed part via the restatement, fed with xn (exact fp64 rows)
+    # the excerpt's RMSNorm in torch: float32 row, variance (the exact mean of
+    # squares rounded to float32), h * rsqrt(variance + eps), cast to bf16, times the bf16 gain
+    h32 = inp.x.float()
+    variance = (h * h).mean(dim=1, keepdim=True).float()
+    normed = (h32 * (1.0 / torch.sqrt(variance + inp.eps))).to(torch.bfloat16)
+    xn = (inp.gain.to(torch.bfloat16) * normed).double()
+    # routed part via the restatement, fed with xn
     n, k = inp.topk_ids.shape
     routed = torch.zeros(n, wl.d, dtype=torch.float64)
     for t in range(n):
