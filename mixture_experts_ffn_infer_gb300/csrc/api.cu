@@ -269,21 +269,25 @@ moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t exper
 }
 
 // The expert pass on an already-sorted routing plan: gather, gate/up, down.
-// `gather` selects the bf16 row gather (moe_experts_forward / moe_infer: two
-// terms carry a bf16 value); the fused layer writes the sorted rows itself
-// (RMSNorm scatter, three terms).
+// `gather` selects the bf16 row gather (moe_experts_forward / moe_infer); the
+// fused layer writes the sorted rows itself (RMSNorm scatter).  Either way the
+// rows are bf16 values, which two e4m3 terms hold.
+// inv_ready: the workspace's inv_pos already holds the inverse of sorted_pos
+// (written by the routing kernel); otherwise the gather derives it first.
 moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float* topk_weight,
                         const int32_t* offsets, const int32_t* sorted_pos, const moe_weights* w, void* rows,
-                        void* ws, const Layout& L, bool gather, cudaStream_t s, Tracer& tr) {
+                        void* ws, const Layout& L, bool gather, bool inv_ready, cudaStream_t s, Tracer& tr) {
   const int32_t R = static_cast<int32_t>(n * d->top_k);
   uint8_t* xs = at<uint8_t>(ws, L.xs);
   float* xs_inv = at<float>(ws, L.xs_inv);
   TileDesc* tiles = at<TileDesc>(ws, L.tiles);
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
-  const int x_terms = gather ? 2 : 3;
+  const int x_terms = 2;
   if (gather) {
-    MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), sorted_pos, R, d->top_k, d->d, xs,
-                                      rows_layout(R, d->num_experts, d->d, x_terms), xs_inv, s));
+    int32_t* ip = at<int32_t>(ws, L.inv_pos);
+    if (!inv_ready) MOE_CHECK_CUDA(launch_invert_positions(sorted_pos, R, ip, s));
+    MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), ip, static_cast<int32_t>(n), d->top_k, d->d,
+                                      xs, rows_layout(R, d->num_experts, d->d, x_terms), xs_inv, s));
     tr.after("gather_rows");
   }
   MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
@@ -300,7 +304,7 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
   MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), tile_tokens(n, 1), tiles, n_tiles, s));
   tr.after("shared_tiles");
-  return run_gemms(w, d->d, dff_sh, 1, static_cast<int32_t>(n), 3, at<uint8_t>(ws, L.xs_sh),
+  return run_gemms(w, d->d, dff_sh, 1, static_cast<int32_t>(n), 2, at<uint8_t>(ws, L.xs_sh),
                    at<float>(ws, L.xs_sh_inv), at<uint8_t>(ws, L.h_sh), at<float>(ws, L.h_sh_inv), tiles, n_tiles,
                    nullptr, nullptr, at<uint16_t>(ws, L.sh_out), at<uint32_t>(ws, L.err), s, tr, "shared_gateup",
                    "shared_down");
@@ -410,7 +414,7 @@ moe_status moe_experts_forward(const moe_dims* dims, int64_t n, const void* x, c
       !aligned(rows, 16))
     return MOE_ERR_INVALID_ARG;
   Tracer tr{nullptr, s};
-  return experts_pass(dims, n, x, topk_weight, expert_offsets, sorted_pos, w, rows, ws, L, true, s, tr);
+  return experts_pass(dims, n, x, topk_weight, expert_offsets, sorted_pos, w, rows, ws, L, true, false, s, tr);
 }
 
 moe_status moe_combine(const moe_dims* dims, int64_t n, const void* rows, const void* shared, const void* residual,
@@ -449,7 +453,7 @@ moe_status moe_infer(const moe_dims* dims, int64_t n, const void* x, const int32
                                       offsets, sp, ip, 0, err, s));
   tr.after("route_permute");
   void* rows = at<void>(ws, L.rows);
-  moe_status st = experts_pass(dims, n, x, topk_weight, offsets, sp, w, rows, ws, L, true, s, tr);
+  moe_status st = experts_pass(dims, n, x, topk_weight, offsets, sp, w, rows, ws, L, true, true, s, tr);
   if (st != MOE_OK) return st;
   MOE_CHECK_CUDA(launch_combine(static_cast<const uint16_t*>(rows), nullptr, nullptr, static_cast<int32_t>(n),
                                 dims->top_k, dims->d, out, out_is_fp32, s));
@@ -484,12 +488,12 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
   const int64_t R = n * dims->top_k;
   MOE_CHECK_CUDA(launch_rmsnorm_scatter(
       static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain), eps, static_cast<int32_t>(n), dims->d,
-      dims->top_k, ip, at<uint8_t>(ws, L.xs), rows_layout(R, dims->num_experts, dims->d, 3), at<float>(ws, L.xs_inv),
-      shared ? at<uint8_t>(ws, L.xs_sh) : nullptr, rows_layout(n, 1, dims->d, 3),
+      dims->top_k, ip, at<uint8_t>(ws, L.xs), rows_layout(R, dims->num_experts, dims->d, 2), at<float>(ws, L.xs_inv),
+      shared ? at<uint8_t>(ws, L.xs_sh) : nullptr, rows_layout(n, 1, dims->d, 2),
       shared ? at<float>(ws, L.xs_sh_inv) : nullptr, s));
   tr.after("rmsnorm_scatter");
   void* rows = at<void>(ws, L.rows);
-  moe_status st = experts_pass(dims, n, nullptr, topk_weight, offsets, sp, routed, rows, ws, L, false, s, tr);
+  moe_status st = experts_pass(dims, n, nullptr, topk_weight, offsets, sp, routed, rows, ws, L, false, true, s, tr);
   if (st != MOE_OK) return st;
   if (shared) {
     st = shared_pass(dims, n, shared, dff_sh, ws, L, s, tr);

@@ -86,9 +86,12 @@ cudaError_t launch_bounded_wait_selftest(uint32_t* err, cudaStream_t s);
 cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles, cudaStream_t s);
 
 // elementwise.cu
-// Sorted activation rows in the split format: codes [3 R][d] e4m3 + exponents [d/128][R].
-cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k,
-                               int32_t d, uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s);
+// Sorted activation rows in the split format from the bf16 tokens: inv_pos [n k]
+// gives each routed slot's sorted position (-1: none).
+cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* inv_pos, int32_t n, int32_t k, int32_t d,
+                               uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s);
+// inv_pos from sorted_pos (entries that no sorted row names become -1).
+cudaError_t launch_invert_positions(const int32_t* sorted_pos, int32_t R, int32_t* inv, cudaStream_t s);
 cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_bf16, float eps, int32_t n,
                                    int32_t d, int32_t k, const int32_t* inv_pos, uint8_t* xs, SplitLayout lay,
                                    float* xs_inv, uint8_t* xs_shared, SplitLayout lay_shared, float* xs_shared_inv,

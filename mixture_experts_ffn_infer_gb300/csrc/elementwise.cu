@@ -1,12 +1,15 @@
 // Bandwidth-bound steps around the grouped GEMMs.
 //
 // gather_rows_kernel    - "Mixture of experts" page, moe_infer: sorted_tokens
-//                         = x[idxs // k]; rows are written in the three-term
-//                         e4m3 split format the GEMMs read (split3.cuh).
+//                         = x[idxs // k]; each token's row is split once into
+//                         the e4m3 split format the GEMMs read (split3.cuh) and
+//                         written to all of its sorted positions.
 // rmsnorm_scatter_kernel- "Input features" page, RMSNorm: fp32 mean of squares,
-//                         rsqrt(mean + eps), times gain; the normalised row is
-//                         split once and written per routed slot straight to its
-//                         sorted position (inv_pos) and to the shared expert's rows.
+//                         h / sqrt(mean + eps) cast to bf16, times the bf16 gain
+//                         in bf16; the normalised row is split once (two terms
+//                         hold a bf16 value) and written per routed slot straight
+//                         to its sorted position (inv_pos) and to the shared
+//                         expert's rows.
 // pack_tiles_kernel     - storage layout only: copies each 128 x 128 tile of
 //                         e4m3 codes into one contiguous 16 KB block, laid out
 //                         exactly as a 128-byte-swizzled TMA box lands in
@@ -28,6 +31,8 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -38,26 +43,50 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
 
 constexpr int kRowThreads = 256;  // eight warps per row, one 128-column block per warp at a time
 
+// One CTA per token: the token's row is read once, each 128-column block is
+// split once and written to every sorted position of the token (inv_pos).
+// Each warp keeps four blocks' loads in flight before it converts them.
 __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t* __restrict__ x,
-                                                                  const int32_t* __restrict__ sorted_pos, int32_t R,
+                                                                  const int32_t* __restrict__ inv_pos, int32_t n,
                                                                   int32_t k, int32_t d, uint8_t* __restrict__ xs,
                                                                   SplitLayout lay, float* __restrict__ xs_inv) {
-  const int64_t i = blockIdx.x;
+  const int64_t t = blockIdx.x;
+  const int64_t R = static_cast<int64_t>(n) * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = sorted_pos[i];
-  const uint16_t* src = p >= 0 ? x + static_cast<int64_t>(p / k) * d : nullptr;
-  for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (src) {
-      const uint2 w = reinterpret_cast<const uint2*>(src + kb * 128)[lane];
-      v[0] = bf16_lo(w.x);
-      v[1] = bf16_hi(w.x);
-      v[2] = bf16_lo(w.y);
-      v[3] = bf16_hi(w.y);
+  int32_t dst_rows[32];
+  int ndst = 0;
+  for (int j = 0; j < k; ++j) {
+    const int p = inv_pos[t * k + j];
+    if (p >= 0 && p < R) dst_rows[ndst++] = p;
+  }
+  if (ndst == 0) return;
+  const uint2* src = reinterpret_cast<const uint2*>(x + t * d);
+  const int nkb = d / 128;
+  constexpr int kWarps = kRowThreads / 32, kBatch = 4;
+  for (int kb0 = warp; kb0 < nkb; kb0 += kWarps * kBatch) {
+    uint2 w[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int kb = kb0 + kWarps * i;
+      w[i] = kb < nkb ? src[kb * 32 + lane] : make_uint2(0u, 0u);
     }
-    uint32_t t1, t2, t3;
-    const float inv = warp_split_block(v, t1, t2, t3);
-    warp_store_block(xs, lay, xs_inv, R, i, kb, t1, t2, t3, inv, lane);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int kb = kb0 + kWarps * i;
+      if (kb >= nkb) break;
+      const float v[4] = {bf16_lo(w[i].x), bf16_hi(w[i].x), bf16_lo(w[i].y), bf16_hi(w[i].y)};
+      uint32_t t1, t2, t3;
+      const float inv = warp_split_block(v, t1, t2, t3);
+      for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
+    }
+  }
+}
+
+// inv[sorted_pos[i]] = i for every valid entry; the rest stay -1 (set before).
+__global__ void invert_positions_kernel(const int32_t* __restrict__ sorted_pos, int32_t R, int32_t* __restrict__ inv) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R; i += gridDim.x * blockDim.x) {
+    const int p = sorted_pos[i];
+    if (p >= 0 && p < R) inv[p] = i;
   }
 }
 
@@ -89,7 +118,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
   if (threadIdx.x == 0) {
     float tot = 0.f;
     for (int w = 0; w < kRowThreads / 32; ++w) tot += red[w];
-    s_inv = rsqrtf(tot / static_cast<float>(d) + eps);
+    s_inv = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
   }
   __syncthreads();
   const float inv_rms = s_inv;
@@ -104,11 +133,12 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
   for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
     const uint2 w = reinterpret_cast<const uint2*>(h + t * d + kb * 128)[lane];
     const uint2 g = reinterpret_cast<const uint2*>(gain + kb * 128)[lane];
+    // the normalised row is cast to bf16, then multiplied by the bf16 gain in bf16
     float v[4];
-    v[0] = bf16_lo(g.x) * (bf16_lo(w.x) * inv_rms);
-    v[1] = bf16_hi(g.x) * (bf16_hi(w.x) * inv_rms);
-    v[2] = bf16_lo(g.y) * (bf16_lo(w.y) * inv_rms);
-    v[3] = bf16_hi(g.y) * (bf16_hi(w.y) * inv_rms);
+    v[0] = bf16_round(bf16_lo(g.x) * bf16_round(bf16_lo(w.x) * inv_rms));
+    v[1] = bf16_round(bf16_hi(g.x) * bf16_round(bf16_hi(w.x) * inv_rms));
+    v[2] = bf16_round(bf16_lo(g.y) * bf16_round(bf16_lo(w.y) * inv_rms));
+    v[3] = bf16_round(bf16_hi(g.y) * bf16_round(bf16_hi(w.y) * inv_rms));
     uint32_t t1, t2, t3;
     const float inv = warp_split_block(v, t1, t2, t3);
     for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
@@ -196,10 +226,19 @@ cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_expe
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* sorted_pos, int32_t R, int32_t k, int32_t d,
+cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* inv_pos, int32_t n, int32_t k, int32_t d,
                                uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  gather_rows_kernel<<<n, kRowThreads, 0, s>>>(x_bf16, inv_pos, n, k, d, xs, lay, xs_inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_invert_positions(const int32_t* sorted_pos, int32_t R, int32_t* inv, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
-  gather_rows_kernel<<<R, kRowThreads, 0, s>>>(x_bf16, sorted_pos, R, k, d, xs, lay, xs_inv);
+  cudaError_t e = cudaMemsetAsync(inv, 0xff, sizeof(int32_t) * static_cast<size_t>(R), s);
+  if (e != cudaSuccess) return e;
+  const int blocks = min((R + 255) / 256, 4096);
+  invert_positions_kernel<<<blocks, 256, 0, s>>>(sorted_pos, R, inv);
   return cudaGetLastError();
 }
 

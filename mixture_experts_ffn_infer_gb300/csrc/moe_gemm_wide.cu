@@ -515,11 +515,11 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
 }  // namespace
 
 // Stages: three weight stages of 32 KB (both blocks of one K block) and
-// activation stages of terms x 16 KB (three of 32 KB for two terms, two of
-// 48 KB for three); about 195 KB of shared memory.
+// activation stages of terms x 16 KB (three of 32 KB for the two terms of the
+// bf16 features, two of 48 KB for the three terms of h); about 195 KB of
+// shared memory.
 cudaError_t launch_gateup_wide(const GemmLaunch& g, cudaStream_t s) {
   if (g.terms == 2) return launch_wide<true, 2, 3, 3>(g, s);
-  if (g.terms == 3) return launch_wide<true, 3, 3, 2>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down_wide(const GemmLaunch& g, cudaStream_t s) {

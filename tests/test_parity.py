@@ -110,9 +110,8 @@ def test_layer_forward_small_with_shared_expert():
     _assert_ok(y2, ref2)
 
 
-def test_layer_forward_wide_tiles_three_terms():
-    # 200 routed rows per expert and 300 shared rows: tiles of 128 rows, the
-    # normalised features in three terms
+def test_layer_forward_wide_tiles():
+    # 200 routed rows per expert and 300 shared rows: tiles of 128 rows
     wl = syn.Workload("blkw", 300, 384, 256, 3, 2, full_block=True, d_ff_shared=256, seed=11)
     c = cases.workload(wl)
     ref = oracle.layer_forward(c.inp.x, c.inp.gain, c.inp.eps, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank,
