@@ -113,17 +113,17 @@ class ClockSampler:
 
 
 def _traffic(workload, kernel):
-    """DRAM bytes per launch from the committed ncu summary, or None when the GEMM source
-    has changed since those counters were taken."""
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel's
+    source file has changed since those counters were taken."""
     import hashlib
     prof = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
-    src = os.path.join(ROOT, "mixture_experts_ffn_infer_gb300", "csrc", "moe_gemm.cu")
     try:
         rec = json.load(open(prof))
+        src = os.path.join(ROOT, "mixture_experts_ffn_infer_gb300", "csrc", rec["source"])
         if rec.get("source_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
             return None
         return rec.get(kernel)
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         return None
 
 

@@ -80,14 +80,15 @@ typedef struct {
 
 /* Layout of the e4m3 codes of a bank. */
 #define MOE_LAYOUT_ROW_MAJOR 0  /* [E][rows][cols], as the model stores them */
-#define MOE_LAYOUT_TILED 1      /* moe_pack_weights output: one contiguous 16 KB block per 128 x 128 tile */
+#define MOE_LAYOUT_TILED 1      /* moe_pack_weights output: 16 KB tiles, two per K block of a work unit */
 
 /* One bank of FP8 SwiGLU experts (device pointers).
  *   w_gate, w_up : [E, d_ff, d] e4m3 codes;  s_gate, s_up : [E, d_ff/128, d/128] fp32
  *   w_down       : [E, d, d_ff] e4m3 codes;  s_down       : [E, d/128, d_ff/128] fp32
  * Element (r, c) of a matrix dequantises to e4m3(code[r][c]) * s[r/128][c/128].
- * With layout MOE_LAYOUT_TILED the code arrays hold the same bytes rearranged
- * by moe_pack_weights (same total size); the scales never change layout.
+ * With layout MOE_LAYOUT_TILED the codes are rearranged by moe_pack_weights:
+ * w_gate holds gate and up together, w_up is not read (may be NULL), w_down
+ * holds down (sizes from moe_tiled_bytes); the scales never change layout.
  * For the shared expert E = 1 and d_ff is the d_ff_shared argument. */
 typedef struct {
     const uint8_t *w_gate, *w_up, *w_down;
@@ -113,19 +114,29 @@ typedef struct {
 size_t moe_workspace_size(const moe_dims *dims, int64_t n_tokens, int32_t d_ff_shared);
 
 /* Weight preparation for streaming (no counterpart on the pages: a storage
- * layout, not arithmetic).  Rearranges the e4m3 codes of a row-major bank
- * (src->layout must be MOE_LAYOUT_ROW_MAJOR) into MOE_LAYOUT_TILED: for each
- * matrix, expert e, 128-row block b and 128-column block c, the 16384 codes of
- * that tile become one contiguous block at offset ((e * R/128 + b) * C/128 + c)
- * * 16384, row r of the tile at r * 128 with its 16-byte chunk j stored at
- * chunk position j ^ (r % 8).  A unit of work then streams one contiguous
- * region instead of 128-byte pieces of 128 rows.
+ * layout, not arithmetic).  The GEMMs work on units of one token tile times
+ * two 128-row weight blocks: gate and up of the same rows, or down row blocks
+ * 2p and 2p+1.  The tiled layout stores the two blocks' 128 x 128 tiles of one
+ * K block (128 columns) next to each other, and consecutive K blocks one after
+ * the other, so a unit streams one contiguous region and every copy moves
+ * both blocks at once.  Each 16 KB tile holds row r of the tile at r * 128 with
+ * its 16-byte chunk j at chunk position j ^ (r % 8) (the image a 128-byte-
+ * swizzled TMA box leaves in shared memory).
+ *   gate/up (dst->w_gate): tile (e, b, c, m) at (((e * d_ff/128 + b) * d/128 + c) * 2 + m) * 16384,
+ *     m = 0 gate rows 128b.., m = 1 up rows 128b.., columns 128c..
+ *   down (dst->w_down): with P = ceil(d/256) pairs, tile (e, p, c, m) at
+ *     (((e * P + p) * d_ff/128 + c) * 2 + m) * 16384 holds down rows 128 (2p + m)..,
+ *     columns 128c..; when d/128 is odd the last pair's second tile is zeros.
  *   num_experts, d, d_ff: the bank's sizes (d_ff = d_ff_shared for a shared expert)
- *   src: row-major codes; dst: caller-allocated code buffers of the same sizes
- *        (dst->s_* and dst->layout are not read).  src and dst must not overlap.
+ *   src: row-major codes; dst: caller-allocated buffers of moe_tiled_bytes bytes
+ *        (dst->w_up, dst->s_* and dst->layout are not read).  src and dst must not overlap.
  * Asynchronous on `stream`; call once when the weights are loaded. */
 moe_status moe_pack_weights(int32_t num_experts, int32_t d, int32_t d_ff, const moe_weights *src,
                             const moe_weights *dst, cudaStream_t stream);
+
+/* Bytes of a tiled code buffer: which = 0 for w_gate (gate and up), 2 for
+ * w_down.  0 for unsupported sizes or another `which`. */
+size_t moe_tiled_bytes(int32_t which, int32_t num_experts, int32_t d, int32_t d_ff);
 
 /* Routing plan ("Mixture of experts" page, moe_infer: the per-expert counts
  * and the sort of the flattened ids by expert).

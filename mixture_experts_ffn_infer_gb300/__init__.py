@@ -60,6 +60,7 @@ _lock = threading.Lock()
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_dims), ctypes.c_int64, ctypes.c_int32]),
+    "moe_tiled_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "moe_pack_weights": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(moe_weights),
                                          ctypes.POINTER(moe_weights), ctypes.c_void_p]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 5
@@ -132,8 +133,8 @@ def dims(d: int, d_ff: int, num_experts: int, top_k: int) -> moe_dims:
 def weights(bank) -> moe_weights:
     """moe_weights from an object with w_gate/w_up/w_down/s_gate/s_up/s_down device tensors
     (and an optional ``layout`` attribute, default row-major)."""
-    return moe_weights(*(bank_t.data_ptr() for bank_t in (bank.w_gate, bank.w_up, bank.w_down, bank.s_gate,
-                                                          bank.s_up, bank.s_down)),
+    return moe_weights(*((t.data_ptr() if t is not None else None) for t in (bank.w_gate, bank.w_up, bank.w_down,
+                                                                              bank.s_gate, bank.s_up, bank.s_down)),
                        int(getattr(bank, "layout", MOE_LAYOUT_ROW_MAJOR)))
 
 
@@ -145,6 +146,10 @@ def moe_status_string(status: int) -> str:
 
 def moe_workspace_size(dm: moe_dims, n_tokens: int, d_ff_shared: int = 0) -> int:
     return load_library().moe_workspace_size(ctypes.byref(dm), n_tokens, d_ff_shared)
+
+
+def moe_tiled_bytes(which: int, num_experts: int, d: int, d_ff: int) -> int:
+    return load_library().moe_tiled_bytes(which, num_experts, d, d_ff)
 
 
 def moe_pack_weights(num_experts, d, d_ff, src: moe_weights, dst: moe_weights, stream=None):
@@ -215,21 +220,32 @@ def moe_get_error(ws, stream=None) -> int:
 # ---------------------------------------------------------------- allocating conveniences
 
 class TiledBank:
-    """A bank whose e4m3 codes are in the tiled streaming layout (tensors keep their shapes)."""
+    """A bank whose e4m3 codes are in the tiled streaming layout: w_gate holds gate and up
+    interleaved, w_up is None, w_down holds down row blocks in pairs (flat uint8 tensors)."""
 
     layout = MOE_LAYOUT_TILED
 
-    def __init__(self, w_gate, w_up, w_down, s_gate, s_up, s_down):
-        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+    def __init__(self, w_gate, w_down, s_gate, s_up, s_down, num_experts, d_ff, d):
+        self.w_gate, self.w_up, self.w_down = w_gate, None, w_down
         self.s_gate, self.s_up, self.s_down = s_gate, s_up, s_down
+        self.num_experts, self.d_ff, self.d = num_experts, d_ff, d
+
+
+def bank_sizes(bank):
+    """(num_experts, d_ff, d) of a row-major or tiled bank."""
+    if isinstance(bank, TiledBank):
+        return bank.num_experts, bank.d_ff, bank.d
+    return tuple(bank.w_gate.shape)
 
 
 def pack_bank(bank, stream=None) -> TiledBank:
     """Tiled copy of a row-major bank's codes (scales shared with the source)."""
     import torch
     E, d_ff, d = bank.w_gate.shape
-    out = TiledBank(torch.empty_like(bank.w_gate), torch.empty_like(bank.w_up), torch.empty_like(bank.w_down),
-                    bank.s_gate, bank.s_up, bank.s_down)
+    dev = bank.w_gate.device
+    gu = torch.empty(moe_tiled_bytes(0, E, d, d_ff), dtype=torch.uint8, device=dev)
+    dn = torch.empty(moe_tiled_bytes(2, E, d, d_ff), dtype=torch.uint8, device=dev)
+    out = TiledBank(gu, dn, bank.s_gate, bank.s_up, bank.s_down, E, d_ff, d)
     moe_pack_weights(E, d, d_ff, weights(bank), weights(out), stream)
     return out
 
@@ -261,7 +277,8 @@ def permute(topk_ids, num_experts: int, ws=None, validate=False, stream=None):
 def infer(x, topk_ids, topk_weight, bank, ws=None, out_is_fp32=False, stream=None):
     import torch
     n, d = x.shape
-    dm = moe_dims(d, bank.w_gate.shape[1], bank.w_gate.shape[0], topk_ids.shape[1])
+    E, d_ff, _ = bank_sizes(bank)
+    dm = moe_dims(d, d_ff, E, topk_ids.shape[1])
     if ws is None:
         ws = workspace(dm, n, 0, x.device)
     out = torch.empty(n, d, dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=x.device)
@@ -273,8 +290,9 @@ def layer_forward(hidden, gain, eps, topk_ids, topk_weight, bank, shared=None, w
                   stream=None):
     import torch
     n, d = hidden.shape
-    dm = moe_dims(d, bank.w_gate.shape[1], bank.w_gate.shape[0], topk_ids.shape[1])
-    dff_sh = shared.w_gate.shape[1] if shared is not None else 0
+    E, d_ff, _ = bank_sizes(bank)
+    dm = moe_dims(d, d_ff, E, topk_ids.shape[1])
+    dff_sh = bank_sizes(shared)[1] if shared is not None else 0
     if ws is None:
         ws = workspace(dm, n, dff_sh, hidden.device)
     out = torch.empty(n, d, dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=hidden.device)

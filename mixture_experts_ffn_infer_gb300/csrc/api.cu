@@ -156,9 +156,11 @@ int num_sms() {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool weights_ok(const moe_weights* w) {
-  return w && w->w_gate && w->w_up && w->w_down && w->s_gate && w->s_up && w->s_down && aligned(w->w_gate, 16) &&
-         aligned(w->w_up, 16) && aligned(w->w_down, 16) &&
-         (w->layout == MOE_LAYOUT_ROW_MAJOR || w->layout == MOE_LAYOUT_TILED);
+  if (!w || !w->w_gate || !w->w_down || !w->s_gate || !w->s_up || !w->s_down || !aligned(w->w_gate, 16) ||
+      !aligned(w->w_down, 16))
+    return false;
+  if (w->layout == MOE_LAYOUT_TILED) return true;  // w_up is part of w_gate
+  return w->layout == MOE_LAYOUT_ROW_MAJOR && w->w_up && aligned(w->w_up, 16);
 }
 
 // Weight maps of a bank (row-major only; the tiled layout is read with bulk copies).
@@ -229,8 +231,7 @@ moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t exper
   g.terms = x_terms;
   g.w0 = &m_g;
   g.w1 = &m_u;
-  g.w0_tiled = tiled ? w->w_gate : nullptr;
-  g.w1_tiled = tiled ? w->w_up : nullptr;
+  g.w_tiled = tiled ? w->w_gate : nullptr;
   mx.bind(g);
   g.s0 = w->s_gate;
   g.s1 = w->s_up;
@@ -252,7 +253,7 @@ moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t exper
   q.terms = 3;
   q.w0 = &m_d;
   q.w1 = &m_d;
-  q.w0_tiled = q.w1_tiled = tiled ? w->w_down : nullptr;
+  q.w_tiled = tiled ? w->w_down : nullptr;
   mh.bind(q);
   q.s0 = w->s_down;
   q.s1 = w->s_down;
@@ -365,23 +366,37 @@ size_t moe_workspace_size(const moe_dims* dims, int64_t n_tokens, int32_t d_ff_s
   return L.total;
 }
 
+size_t moe_tiled_bytes(int32_t which, int32_t E, int32_t d, int32_t dff) {
+  if (E < 1 || d <= 0 || dff <= 0 || d % 128 != 0 || dff % 128 != 0) return 0;
+  if (which == 0) return static_cast<size_t>(pack_tile_count(E, dff, d, 0)) * 16384;
+  if (which == 2) return static_cast<size_t>(pack_tile_count(E, d, dff, 1)) * 16384;
+  return 0;
+}
+
 moe_status moe_pack_weights(int32_t E, int32_t d, int32_t dff, const moe_weights* src, const moe_weights* dst,
                             cudaStream_t s) {
   if (!src || !dst) return MOE_ERR_INVALID_ARG;
   if (E < 1 || d <= 0 || dff <= 0 || d % 128 != 0 || dff % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (src->layout != MOE_LAYOUT_ROW_MAJOR) return MOE_ERR_INVALID_ARG;
+  const size_t mat = static_cast<size_t>(E) * d * dff;
   const uint8_t* in[3] = {src->w_gate, src->w_up, src->w_down};
-  const uint8_t* out[3] = {dst->w_gate, dst->w_up, dst->w_down};
-  const int32_t rows[3] = {dff, dff, d}, cols[3] = {d, d, dff};
-  const size_t bytes = static_cast<size_t>(E) * d * dff;
-  for (int m = 0; m < 3; ++m) {
-    if (!in[m] || !out[m] || !aligned(in[m], 16) || !aligned(out[m], 16)) return MOE_ERR_INVALID_ARG;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(in[m]), b0 = reinterpret_cast<uintptr_t>(out[m]);
-    if (a0 < b0 + bytes && b0 < a0 + bytes) return MOE_ERR_INVALID_ARG;  // overlapping buffers
-  }
+  const uint8_t* out[2] = {dst->w_gate, dst->w_down};
+  const size_t out_bytes[2] = {moe_tiled_bytes(0, E, d, dff), moe_tiled_bytes(2, E, d, dff)};
   for (int m = 0; m < 3; ++m)
-    if (launch_pack_tiles(in[m], const_cast<uint8_t*>(out[m]), E, rows[m], cols[m], s) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    if (!in[m] || !aligned(in[m], 16)) return MOE_ERR_INVALID_ARG;
+  for (int o = 0; o < 2; ++o) {
+    if (!out[o] || !aligned(out[o], 16)) return MOE_ERR_INVALID_ARG;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(out[o]);
+    for (int m = 0; m < 3; ++m) {  // no source may overlap a destination
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(in[m]);
+      if (a0 < b0 + out_bytes[o] && b0 < a0 + mat) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  const uintptr_t g0 = reinterpret_cast<uintptr_t>(out[0]), d0 = reinterpret_cast<uintptr_t>(out[1]);
+  if (g0 < d0 + out_bytes[1] && d0 < g0 + out_bytes[0]) return MOE_ERR_INVALID_ARG;
+  if (launch_pack_tiles(in[0], in[1], const_cast<uint8_t*>(out[0]), E, dff, d, 0, s) != cudaSuccess ||
+      launch_pack_tiles(in[2], nullptr, const_cast<uint8_t*>(out[1]), E, d, dff, 1, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -96,8 +96,11 @@ cudaError_t launch_rmsnorm_scatter(const uint16_t* h_bf16, const uint16_t* gain_
                                    int32_t d, int32_t k, const int32_t* inv_pos, uint8_t* xs, SplitLayout lay,
                                    float* xs_inv, uint8_t* xs_shared, SplitLayout lay_shared, float* xs_shared_inv,
                                    cudaStream_t s);
-cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_experts, int32_t rows, int32_t cols,
-                              cudaStream_t s);
+// Tiled layout (moe_pack_weights): paired = 0 interleaves src0 and src1 (gate, up)
+// per row block; paired = 1 interleaves row blocks 2u, 2u + 1 of src0 (down).
+int64_t pack_tile_count(int32_t num_experts, int32_t rows, int32_t cols, int32_t paired);
+cudaError_t launch_pack_tiles(const uint8_t* src0, const uint8_t* src1, uint8_t* dst, int32_t num_experts,
+                              int32_t rows, int32_t cols, int32_t paired, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* rows_f16, const uint16_t* shared_f16, const uint16_t* resid_bf16,
                            int32_t n, int32_t k, int32_t d, void* out, int32_t out_fp32, cudaStream_t s);
 
@@ -110,13 +113,16 @@ struct GemmLaunch {
   const CUtensorMap* act_box;   // wide tiles: 3-D map over [terms][rows][K], box 128 x 128 rows x terms
   int32_t ntok;                 // token tile width (kNTokSmall or kNTokWide)
   int32_t terms;                // wide tiles: activation terms (2 or 3)
-  const uint8_t* w0_tiled;      // tiled layout (moe_pack_weights): used instead of w0 / w1 when non-null
-  const uint8_t* w1_tiled;
+  // Tiled layout (moe_pack_weights): both weight blocks of a unit per K block, 32 KB,
+  // consecutive K blocks contiguous; used instead of w0 / w1 when non-null.
+  const uint8_t* w_tiled;
   const float* s0;              // scales [E][n_nb][num_kb]
   const float* s1;
   const TileDesc* tiles;
   const int32_t* n_tiles;
   int32_t n_nb;                 // weight-row blocks of 128 (output features / 128)
+  // A unit is one token tile times two weight blocks: gate/up pass = row block j
+  // of w0 and of w1; down pass = row blocks 2j and 2j + 1 of w0.
   int32_t num_kb;               // K / 128
   const float* act_inv;         // [num_kb][act_rows] 2^-s of each activation block
   int32_t act_rows;             // rows of the sorted activation matrix

@@ -13,7 +13,8 @@
 // pack_tiles_kernel     - storage layout only: copies each 128 x 128 tile of
 //                         e4m3 codes into one contiguous 16 KB block, laid out
 //                         exactly as a 128-byte-swizzled TMA box lands in
-//                         shared memory, so the GEMM streams it with one bulk copy.
+//                         shared memory, the two weight blocks of a GEMM unit
+//                         side by side per K block, so one bulk copy moves both.
 // combine_kernel        - "Mixture of experts" page, moe_infer: sum of the
 //                         token's k weighted rows (fp32, ascending slot), plus
 //                         the shared expert ("forward") and the residual
@@ -198,31 +199,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
-// One CTA per tile; tiles enumerated ((expert * rows/128 + row block) * cols/128 + col block).
-__global__ void __launch_bounds__(256) pack_tiles_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                                         int32_t rows, int32_t cols) {
+// One CTA per 16 KB output tile; tiles enumerated (((e * unit_rows + u) * cols/128 + c) * 2 + m).
+// Source row block of tile (u, m): gate/up (paired = 0): block u of src_m;
+// down (paired = 1): block 2u + m of src0, zeros past the last block.
+__global__ void __launch_bounds__(256) pack_tiles_kernel(const uint8_t* __restrict__ src0,
+                                                         const uint8_t* __restrict__ src1, uint8_t* __restrict__ dst,
+                                                         int32_t rows, int32_t cols, int32_t paired) {
   const int64_t t = blockIdx.x;
   const int nrb = rows / 128, ncb = cols / 128;
-  const int64_t e = t / (static_cast<int64_t>(nrb) * ncb);
-  const int rem = static_cast<int>(t - e * nrb * ncb);
-  const int b = rem / ncb, c = rem % ncb;
-  const uint8_t* s = src + (e * rows + static_cast<int64_t>(b) * 128) * cols + static_cast<int64_t>(c) * 128;
+  const int unit_rows = paired ? (nrb + 1) / 2 : nrb;
+  const int m = static_cast<int>(t & 1);
+  const int64_t q = t >> 1;  // (e * unit_rows + u) * ncb + c
+  const int c = static_cast<int>(q % ncb);
+  const int64_t eu = q / ncb;
+  const int u = static_cast<int>(eu % unit_rows);
+  const int64_t e = eu / unit_rows;
+  const int b = paired ? 2 * u + m : u;
+  const uint8_t* src = paired ? src0 : (m ? src1 : src0);
   uint8_t* d = dst + t * 16384;
-  for (int q = threadIdx.x; q < 1024; q += 256) {
-    const int r = q >> 3, j = q & 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(s + static_cast<int64_t>(r) * cols + j * 16);
+  for (int i = threadIdx.x; i < 1024; i += 256) {
+    const int r = i >> 3, j = i & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (b < nrb)
+      v = *reinterpret_cast<const uint4*>(src + (e * rows + static_cast<int64_t>(b) * 128 + r) * cols +
+                                          static_cast<int64_t>(c) * 128 + j * 16);
     *reinterpret_cast<uint4*>(d + r * 128 + ((j ^ (r & 7)) << 4)) = v;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_pack_tiles(const uint8_t* src, uint8_t* dst, int32_t num_experts, int32_t rows, int32_t cols,
-                              cudaStream_t s) {
-  const int64_t tiles = static_cast<int64_t>(num_experts) * (rows / 128) * (cols / 128);
+int64_t pack_tile_count(int32_t num_experts, int32_t rows, int32_t cols, int32_t paired) {
+  const int64_t nrb = rows / 128;
+  return static_cast<int64_t>(num_experts) * (paired ? (nrb + 1) / 2 : nrb) * (cols / 128) * 2;
+}
+
+cudaError_t launch_pack_tiles(const uint8_t* src0, const uint8_t* src1, uint8_t* dst, int32_t num_experts,
+                              int32_t rows, int32_t cols, int32_t paired, cudaStream_t s) {
+  const int64_t tiles = pack_tile_count(num_experts, rows, cols, paired);
   if (tiles <= 0) return cudaSuccess;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  pack_tiles_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(src, dst, rows, cols);
+  pack_tiles_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(src0, src1, dst, rows, cols, paired);
   return cudaGetLastError();
 }
 

@@ -9,20 +9,22 @@
 // scale per 128 x 128 block.
 //
 // One persistent CTA per SM walks a list of work units.  A unit is one tile of
-// at most NTOK sorted rows of one expert times one block of 128 weight rows
-// (128 output features).  The weights are the MMA's M side (128 rows) and the
-// tokens its N side ("swap AB").  The e4m3 weight tiles go from global memory
-// to shared memory by bulk copy (tiled layout) or TMA (row-major layout) and
+// at most NTOK sorted rows of one expert times two blocks of 128 weight rows:
+// gate and up of the same 128 output features (gate/up pass), or down row
+// blocks 2j and 2j + 1 (down pass).  The weights are the MMA's M side (128
+// rows) and the tokens its N side ("swap AB").  The e4m3 weight tiles go from
+// global memory to shared memory by bulk copy (tiled layout: both blocks of
+// KPS consecutive K blocks in one copy) or TMA (row-major layout) and
 // straight into tcgen05.mma kind::f8f6f4 - no conversion.  The activations
 // arrive in the three-term e4m3 split format (split3.cuh): the N side of each
 // MMA holds the three terms of NTOK tokens (N = 3 NTOK).  Per 128-wide K block:
 //
-//   warp 0      weight producer: tile(s) of 16 KB into a ring of stages, L2
-//               prefetch a few blocks ahead.
+//   warp 0      weight producer: stages of KPS K blocks x both weight blocks
+//               into a ring, L2 prefetch a few stages ahead.
 //   warp 2      activation producer: the block of 3 NTOK rows x 128 bytes
 //               into its own ring, so neither ring throttles the other.
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=3 NTOK, K=32) per
-//               matrix into a fresh fp32 partial in tensor memory.
+//               weight block into a fresh fp32 partial in tensor memory.
 //   warps 4-7   epilogue: per token, sum the three term columns, multiply by
 //               the weight block's fp32 scale and the activation block's 2^-s
 //               and add to fp32 accumulators in registers - the exact
@@ -31,7 +33,7 @@
 // After the last K block the epilogue writes, per valid token column,
 //   gate/up pass : h = silu(g) * u in the split format (one block scale per
 //                  row and 128 features, found with a max over the 4 warps)
-//   down pass    : f16(topk_weight * o) -> rows[flat position][feature]
+//   down pass    : f16(topk_weight * o) -> rows[flat position][feature], both blocks
 //
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag and
 // the device error word, the roles drain their in-flight copies and MMAs and
@@ -57,14 +59,14 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int NMAT, int NTOK, int KPS, int WST, int BST, int DST>
+template <int NTOK, int KPS, int WST, int BST, int DST>
 struct Cfg {
   static constexpr int kNB = 3 * NTOK;                   // MMA N: three e4m3 terms per token
   static constexpr int kWTile = 128 * 128;               // e4m3 weight tile bytes
-  static constexpr int kWMat = KPS * kWTile;             // KPS consecutive K blocks of one matrix
-  static constexpr int kWStage = NMAT * kWMat;           // one weight stage (gate + up, or down)
+  static constexpr int kWKb = 2 * kWTile;                // both weight blocks of one K block
+  static constexpr int kWStage = KPS * kWKb;             // one weight stage: [K block][block][tile]
   static constexpr int kBStage = kNB * 128;              // one K block of split activations
-  static constexpr int kDCols = NMAT * kNB;              // tensor-memory columns of one partial buffer
+  static constexpr int kDCols = 2 * kNB;                 // tensor-memory columns of one partial buffer
   static constexpr int kTmemCols = pow2_at_least(DST * kDCols);
   static constexpr int kNumBars = 2 * WST + 2 * BST + 2 * DST + 2 + 1;
   static constexpr int kBOffset = WST * kWStage;
@@ -80,14 +82,14 @@ struct Cfg {
 };
 
 struct GemmArgs {
-  const uint8_t* w0_tiled;  // non-null: weights in the tiled layout, streamed with bulk copies
-  const uint8_t* w1_tiled;
-  const float* s0;
+  const uint8_t* w_tiled;   // non-null: weights in the tiled layout, streamed with bulk copies
+  const float* s0;          // scales of block 0 / block 1 [E][n_nb][num_kb]
   const float* s1;
   const TileDesc* tiles;
   const int32_t* n_tiles;
   int32_t n_nb;
   int32_t num_kb;
+  int32_t pair;             // 1: unit = row blocks 2j, 2j + 1 of w0 (down); 0: row block j of w0 and w1
   const float* act_inv;     // [num_kb][act_rows]: 2^-s of each activation block
   int32_t act_rows;
   void* out;                // gate/up: h terms [3 act_rows][n_nb*128] e4m3; down: rows [.][n_nb*128] f16
@@ -96,6 +98,21 @@ struct GemmArgs {
   const float* topk_weight;
   uint32_t* err;
 };
+
+struct Unit16 {
+  int e, ru, nb0, nb1;
+  bool has1;
+};
+
+__device__ __forceinline__ Unit16 unit16(const GemmArgs& a, const TileDesc& td, int u, int upt) {
+  Unit16 x;
+  x.e = td.expert;
+  x.ru = u % upt;
+  x.nb0 = a.pair ? 2 * x.ru : x.ru;
+  x.nb1 = a.pair ? 2 * x.ru + 1 : x.ru;
+  x.has1 = x.nb1 < a.n_nb;
+  return x;
+}
 
 // Bounded wait used while winding down: ignores the abort flag.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
@@ -114,11 +131,11 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-template <int NMAT, int NTOK, int KPS, int WST, int BST, int DST>
+template <bool GATEUP, int NTOK, int KPS, int WST, int BST, int DST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                 const __grid_constant__ CUtensorMap tm_act, const GemmArgs a) {
-  using C = Cfg<NMAT, NTOK, KPS, WST, BST, DST>;
+  using C = Cfg<NTOK, KPS, WST, BST, DST>;
   constexpr int NB = C::kNB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,9 +175,9 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     fence_mbar_init();
   }
   if (warp == kWarpProducer && lane == 0) {
-    if (!a.w0_tiled) {
+    if (!a.w_tiled) {
       prefetch_tmap(&tm_w0);
-      if (NMAT == 2) prefetch_tmap(&tm_w1);
+      prefetch_tmap(&tm_w1);
     }
     prefetch_tmap(&tm_act);
   }
@@ -174,26 +191,29 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   const uint32_t tmem = *tmem_slot;
 
   const int n_nb = a.n_nb, num_kb = a.num_kb;
-  const int total_units = *a.n_tiles * n_nb;
+  const int upt = a.pair ? (n_nb + 1) / 2 : n_nb;  // units per tile
+  const int total_units = *a.n_tiles * upt;
+  // tiled layout: K block kb of unit row ru of expert e, both blocks (32 KB)
+  auto unit_off = [&](int e, int ru, int kb) {
+    return ((static_cast<int64_t>(e) * upt + ru) * num_kb + kb) * C::kWKb;
+  };
 
   if (warp == kWarpProducer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       // L2 prefetch cursor, kPrefetch stages ahead of the loads
-      int pf_u = blockIdx.x, pf_kb = 0, pf_e = 0;
+      int pf_u = blockIdx.x, pf_kb = 0;
+      Unit16 pf{};
       auto prefetch_one = [&]() {
         if (pf_u >= total_units) return;
-        if (pf_kb == 0) pf_e = a.tiles[pf_u / n_nb].expert;
-        const int nb = pf_u % n_nb;
+        if (pf_kb == 0) pf = unit16(a, a.tiles[pf_u / upt], pf_u, upt);
         const int nk = min(KPS, num_kb - pf_kb);
-        if (a.w0_tiled) {
-          const int64_t toff = ((static_cast<int64_t>(pf_e) * n_nb + nb) * num_kb + pf_kb) * C::kWTile;
-          bulk_prefetch_l2(a.w0_tiled + toff, nk * C::kWTile);
-          if (NMAT == 2) bulk_prefetch_l2(a.w1_tiled + toff, nk * C::kWTile);
+        if (a.w_tiled) {
+          bulk_prefetch_l2(a.w_tiled + unit_off(pf.e, pf.ru, pf_kb), nk * C::kWKb);
         } else {
           for (int j = 0; j < nk; ++j) {
-            tma_prefetch_3d(&tm_w0, (pf_kb + j) * 128, nb * 128, pf_e);
-            if (NMAT == 2) tma_prefetch_3d(&tm_w1, (pf_kb + j) * 128, nb * 128, pf_e);
+            tma_prefetch_3d(&tm_w0, (pf_kb + j) * 128, pf.nb0 * 128, pf.e);
+            if (pf.has1) tma_prefetch_3d(&tm_w1, (pf_kb + j) * 128, pf.nb1 * 128, pf.e);
           }
         }
         pf_kb += nk;
@@ -206,8 +226,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       uint32_t w_issued = 0;  // weight stages issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int e = a.tiles[u / n_nb].expert;
-        const int nb = u % n_nb;
+        const Unit16 un = unit16(a, a.tiles[u / upt], u, upt);
         for (int kb = 0; kb < num_kb; kb += KPS) {
           const uint32_t it = w_issued;
           const int sw = it % WST;
@@ -217,18 +236,18 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             break;
           }
           const uint32_t wst = sbase + sw * C::kWStage;
-          mbar_arrive_expect_tx(full_w(sw), NMAT * nk * C::kWTile);
-          if (a.w0_tiled) {
-            // the stage's K blocks are consecutive 16 KB tiles, already in the swizzled
-            // image: one bulk copy of up to KPS tiles per matrix
-            const int64_t toff = ((static_cast<int64_t>(e) * n_nb + nb) * num_kb + kb) * C::kWTile;
-            bulk_load(wst, a.w0_tiled + toff, nk * C::kWTile, full_w(sw), pol_w);
-            if (NMAT == 2) bulk_load(wst + C::kWMat, a.w1_tiled + toff, nk * C::kWTile, full_w(sw), pol_w);
+          if (a.w_tiled) {
+            // the stage's K blocks, both weight blocks each, are one contiguous
+            // region already in the swizzled image: one bulk copy
+            mbar_arrive_expect_tx(full_w(sw), nk * C::kWKb);
+            bulk_load(wst, a.w_tiled + unit_off(un.e, un.ru, kb), nk * C::kWKb, full_w(sw), pol_w);
           } else {
+            mbar_arrive_expect_tx(full_w(sw), nk * (un.has1 ? 2 : 1) * C::kWTile);
             for (int j = 0; j < nk; ++j) {
-              tma_load_3d(wst + j * C::kWTile, &tm_w0, full_w(sw), (kb + j) * 128, nb * 128, e, pol_w);
-              if (NMAT == 2)
-                tma_load_3d(wst + C::kWMat + j * C::kWTile, &tm_w1, full_w(sw), (kb + j) * 128, nb * 128, e, pol_w);
+              tma_load_3d(wst + j * C::kWKb, &tm_w0, full_w(sw), (kb + j) * 128, un.nb0 * 128, un.e, pol_w);
+              if (un.has1)
+                tma_load_3d(wst + j * C::kWKb + C::kWTile, &tm_w1, full_w(sw), (kb + j) * 128, un.nb1 * 128, un.e,
+                            pol_w);
             }
           }
           ++w_issued;
@@ -246,7 +265,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       uint32_t b_issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int row0 = a.tiles[u / n_nb].row_start;
+        const int row0 = a.tiles[u / upt].row_start;
         for (int kb = 0; kb < num_kb; ++kb) {
           const uint32_t it = b_issued;
           const int sb = it % BST;
@@ -271,6 +290,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       uint32_t it = 0, wt = 0;  // K blocks and weight stages consumed
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const bool has1 = a.pair ? (2 * (u % upt) + 1 < n_nb) : true;
         for (int kb0 = 0; ok && kb0 < num_kb; kb0 += KPS, ++wt) {
           const int sw = wt % WST;
           const int nk = min(KPS, num_kb - kb0);
@@ -289,9 +309,10 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             tc_fence_after();
             const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-              const uint32_t d_addr = tmem + (sd * NMAT + m) * NB;
-              const uint32_t wtile = wst + m * C::kWMat + j * C::kWTile;
+            for (int m = 0; m < 2; ++m) {
+              if (m == 1 && !has1) break;
+              const uint32_t d_addr = tmem + (sd * 2 + m) * NB;
+              const uint32_t wtile = wst + j * C::kWKb + m * C::kWTile;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 mma_f8_ss(d_addr, desc_kmajor_sw128(wtile + kk * 32), desc_kmajor_sw128(bst + kk * 32), idesc,
@@ -314,20 +335,20 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     uint32_t it = 0, ui = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
-      const TileDesc td = a.tiles[u / n_nb];
-      const int nb = u % n_nb;
-      const float* sc0 = a.s0 + (static_cast<int64_t>(td.expert) * n_nb + nb) * num_kb;
-      const float* sc1 = NMAT == 2 ? a.s1 + (static_cast<int64_t>(td.expert) * n_nb + nb) * num_kb : sc0;
-      float acc[NMAT][NTOK];
+      const TileDesc td = a.tiles[u / upt];
+      const Unit16 un = unit16(a, td, u, upt);
+      const float* sc0 = a.s0 + (static_cast<int64_t>(un.e) * n_nb + un.nb0) * num_kb;
+      const float* sc1 = a.s1 + (static_cast<int64_t>(un.e) * n_nb + (un.has1 ? un.nb1 : un.nb0)) * num_kb;
+      float acc[2][NTOK];
 #pragma unroll
-      for (int m = 0; m < NMAT; ++m)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) acc[m][j] = 0.f;
       // Down pass: destination rows and router weights of the tile, loaded now so their
       // latency hides behind the K loop instead of stalling the end of the unit.
-      int dest[NMAT == 1 ? NTOK : 1];
-      float wgt[NMAT == 1 ? NTOK : 1];
-      if (NMAT == 1) {
+      int dest[GATEUP ? 1 : NTOK];
+      float wgt[GATEUP ? 1 : NTOK];
+      if (!GATEUP) {
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) {
           const int row = td.row_start + j;
@@ -338,7 +359,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
           wgt[j] = (j < td.n_valid && a.topk_weight) ? __ldg(a.topk_weight + dest[j]) : 1.0f;
       }
       // scales of the first K block; each iteration loads the next block's
-      float s0n = __ldg(sc0), s1n = NMAT == 2 ? __ldg(sc1) : 0.f;
+      float s0n = __ldg(sc0), s1n = __ldg(sc1);
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int sd = it % DST;
         const float s0v = s0n, s1v = s1n;
@@ -347,7 +368,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         const float* inv = a.act_inv + static_cast<int64_t>(kb) * a.act_rows + td.row_start;
         if (kb + 1 < num_kb) {
           s0n = __ldg(sc0 + kb + 1);
-          if (NMAT == 2) s1n = __ldg(sc1 + kb + 1);
+          s1n = __ldg(sc1 + kb + 1);
           if (lane < (NTOK + 31) / 32 + 1 && td.row_start + lane * 32 < a.act_rows)
             asm volatile("prefetch.global.L1 [%0];" ::"l"(inv + a.act_rows + lane * 32) : "memory");
         }
@@ -360,12 +381,13 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
 #pragma unroll
           for (int j = 0; j < 16; ++j) sx[j] = 16 * c + j < td.n_valid ? __ldg(inv + 16 * c + j) : 0.f;
 #pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
+          for (int m = 0; m < 2; ++m) {
+            if (m == 1 && !un.has1) break;
             const float sv = m == 0 ? s0v : s1v;
             uint32_t p[48];
 #pragma unroll
             for (int c0 = 0; c0 < 48; c0 += 16)
-              tmem_ld16(tmem + lane_base + (sd * NMAT + m) * NB + 48 * c + c0,
+              tmem_ld16(tmem + lane_base + (sd * 2 + m) * NB + 48 * c + c0,
                         *reinterpret_cast<uint32_t(*)[16]>(&p[c0]));
             tmem_ld_wait();
 #pragma unroll
@@ -382,7 +404,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       }
       if (!ok) break;
       bool overflow = false;
-      if (NMAT == 2) {
+      if (GATEUP) {
         // h = silu(g) * u, then the split format with one exponent per (row, 128 features):
         // the block maximum is taken over the 128 threads (4 warps x 32 lanes).
         // The exchange goes through red[ui & 1] and an mbarrier of four arrivals, so a
@@ -392,7 +414,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
 #pragma unroll
         for (int j = 0; j < NTOK; ++j) {
           const float g = acc[0][j];
-          hv[j] = g / (1.0f + expf(-g)) * acc[NMAT - 1][j];
+          hv[j] = g / (1.0f + expf(-g)) * acc[1][j];
           overflow |= (j < td.n_valid) && !isfinite(hv[j]);
           const float m = warp_max(fabsf(hv[j]));
           if (lane == 0) rb[q * NTOK + j] = m;
@@ -411,22 +433,27 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             uint8_t t1, t2, t3;
             split3(ldexpf(hv[j], sexp), t1, t2, t3);
             const int64_t row = td.row_start + j;
-            uint8_t* dst = hterm + (3 * row) * ld + nb * 128 + r;
+            uint8_t* dst = hterm + (3 * row) * ld + un.nb0 * 128 + r;
             dst[0] = t1;
             dst[ld] = t2;
             dst[2 * ld] = t3;
-            if (r == 0) a.out_inv[static_cast<int64_t>(nb) * a.act_rows + row] = ldexpf(1.0f, -sexp);
+            if (r == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = ldexpf(1.0f, -sexp);
           }
         }
       } else {
         uint16_t* rows = static_cast<uint16_t*>(a.out);
         const int64_t ld = static_cast<int64_t>(n_nb) * 128;
 #pragma unroll
-        for (int j = 0; j < NTOK; ++j) {
-          if (j < td.n_valid) {
-            const __half hh = __float2half_rn(acc[0][j] * wgt[NMAT == 1 ? j : 0]);
-            overflow |= __hisinf(hh) != 0 || __hisnan(hh);
-            rows[static_cast<int64_t>(dest[NMAT == 1 ? j : 0]) * ld + nb * 128 + r] = __half_as_ushort(hh);
+        for (int m = 0; m < 2; ++m) {
+          if (m == 1 && !un.has1) break;
+          const int nb = m == 0 ? un.nb0 : un.nb1;
+#pragma unroll
+          for (int j = 0; j < NTOK; ++j) {
+            if (j < td.n_valid) {
+              const __half hh = __float2half_rn(acc[m][j] * wgt[GATEUP ? 0 : j]);
+              overflow |= __hisinf(hh) != 0 || __hisnan(hh);
+              rows[static_cast<int64_t>(dest[GATEUP ? 0 : j]) * ld + nb * 128 + r] = __half_as_ushort(hh);
+            }
           }
         }
       }
@@ -440,21 +467,21 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   }
 }
 
-template <int NMAT, int NTOK, int KPS, int WST, int BST, int DST>
+template <bool GATEUP, int NTOK, int KPS, int WST, int BST, int DST>
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  using C = Cfg<NMAT, NTOK, KPS, WST, BST, DST>;
-  auto kern = moe_gemm_kernel<NMAT, NTOK, KPS, WST, BST, DST>;
+  using C = Cfg<NTOK, KPS, WST, BST, DST>;
+  auto kern = moe_gemm_kernel<GATEUP, NTOK, KPS, WST, BST, DST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   GemmArgs a;
-  a.w0_tiled = g.w0_tiled;
-  a.w1_tiled = g.w1_tiled;
+  a.w_tiled = g.w_tiled;
   a.s0 = g.s0;
   a.s1 = g.s1;
   a.tiles = g.tiles;
   a.n_tiles = g.n_tiles;
   a.n_nb = g.n_nb;
   a.num_kb = g.num_kb;
+  a.pair = GATEUP ? 0 : 1;
   a.act_inv = g.act_inv;
   a.act_rows = g.act_rows;
   a.out = g.out;
@@ -462,7 +489,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;
-  kern<<<g.num_sms, kThreads, C::kSmem, s>>>(*g.w0, NMAT == 2 ? *g.w1 : *g.w0, *g.act, a);
+  kern<<<g.num_sms, kThreads, C::kSmem, s>>>(*g.w0, *g.w1, *g.act, a);
   return cudaGetLastError();
 }
 
@@ -475,16 +502,17 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 // Decode-sized tiles (16 tokens, MMA N = 48):
 //   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 x 6 KB activation stages,
 //            4 partial buffers (384 tensor-memory columns)
-//   down:    3 stages of 4 K blocks = 64 KB, 4 x 6 KB activation stages, 8 partial buffers
+//   down:    3 stages of 2 K blocks x 2 row blocks = 64 KB, 4 x 6 KB activation stages,
+//            4 partial buffers
 // Wide tiles (up to 128 tokens) go to moe_gemm_wide.cu.
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
   if (g.ntok == kNTokWide) return launch_gateup_wide(g, s);
-  if (g.ntok == kNTokSmall) return launch_gemm<2, kNTokSmall, 1, 6, 4, 4>(g, s);
+  if (g.ntok == kNTokSmall) return launch_gemm<true, kNTokSmall, 1, 6, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) {
   if (g.ntok == kNTokWide) return launch_down_wide(g, s);
-  if (g.ntok == kNTokSmall) return launch_gemm<1, kNTokSmall, 4, 3, 4, 8>(g, s);
+  if (g.ntok == kNTokSmall) return launch_gemm<false, kNTokSmall, 2, 3, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 

@@ -28,8 +28,9 @@
 //
 // Warps (384 threads = 3 warpgroups, one CTA per SM, persistent over the unit
 // list; warpgroup 0 hands registers to the epilogue warpgroups):
-//   0      weight producer: the K block's two 16 KB tiles (bulk copies of the
-//          tiled layout, or 3-D TMA of the row-major layout), L2 prefetch ahead
+//   0      weight producer: the K block's two 16 KB tiles (one 32 KB bulk copy
+//          of the tiled layout, or 3-D TMA of the row-major layout), L2
+//          prefetch ahead
 //   1      MMA issuer (one thread)
 //   2      activation producer: one 3-D TMA box [terms][128 rows][128 bytes]
 //          per K block
@@ -77,8 +78,7 @@ struct WideCfg {
 };
 
 struct WideArgs {
-  const uint8_t* w0_tiled;  // non-null: tiled layout, read with bulk copies
-  const uint8_t* w1_tiled;
+  const uint8_t* w_tiled;   // non-null: tiled layout (both blocks of a K block in 32 KB), bulk copies
   const float* s0;          // [E][n_nb][num_kb]
   const float* s1;
   const TileDesc* tiles;
@@ -97,7 +97,7 @@ struct WideArgs {
 };
 
 struct Unit {
-  int e, row0, nv, nb0, nb1;
+  int e, row0, nv, ru, nb0, nb1;
   bool has1;
 };
 
@@ -108,6 +108,7 @@ __device__ __forceinline__ Unit unit_of(const WideArgs& a, int u, int upt) {
   x.e = td.expert;
   x.row0 = td.row_start;
   x.nv = td.n_valid;
+  x.ru = j;
   x.nb0 = a.pair ? 2 * j : j;
   x.nb1 = a.pair ? 2 * j + 1 : j;
   x.has1 = x.nb1 < a.n_nb;
@@ -212,7 +213,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
     fence_mbar_init();
   }
   if (warp == kWarpWeights && lane == 0) {
-    if (!a.w0_tiled) {
+    if (!a.w_tiled) {
       prefetch_tmap(&tm_w0);
       prefetch_tmap(&tm_w1);
     }
@@ -230,8 +231,9 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
   const int n_nb = a.n_nb, num_kb = a.num_kb;
   const int upt = a.pair ? (n_nb + 1) / 2 : n_nb;  // units per tile
   const int total_units = *a.n_tiles * upt;
-  auto tile_off = [&](int e, int nb, int kb) {
-    return ((static_cast<int64_t>(e) * n_nb + nb) * num_kb + kb) * kWTileBytes;
+  // tiled layout: K block kb of unit row ru of expert e, both blocks (32 KB)
+  auto unit_off = [&](int e, int ru, int kb) {
+    return ((static_cast<int64_t>(e) * upt + ru) * num_kb + kb) * (2 * kWTileBytes);
   };
 
   if (warp < kWarpEpi) regs_dec_producer();
@@ -243,9 +245,8 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       auto prefetch_one = [&]() {
         if (pf_u >= total_units) return;
         if (pf_kb == 0) pf = unit_of(a, pf_u, upt);
-        if (a.w0_tiled) {
-          bulk_prefetch_l2(a.w0_tiled + tile_off(pf.e, pf.nb0, pf_kb), kWTileBytes);
-          if (pf.has1) bulk_prefetch_l2(a.w1_tiled + tile_off(pf.e, pf.nb1, pf_kb), kWTileBytes);
+        if (a.w_tiled) {
+          bulk_prefetch_l2(a.w_tiled + unit_off(pf.e, pf.ru, pf_kb), 2 * kWTileBytes);
         } else {
           tma_prefetch_3d(&tm_w0, pf_kb * 128, pf.nb0 * 128, pf.e);
           if (pf.has1) tma_prefetch_3d(&tm_w1, pf_kb * 128, pf.nb1 * 128, pf.e);
@@ -267,12 +268,12 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
             break;
           }
           const uint32_t dst = sbase + sw * C::kWStage;
-          mbar_arrive_expect_tx(full_w(sw), (un.has1 ? 2 : 1) * kWTileBytes);
-          if (a.w0_tiled) {
-            bulk_load(dst, a.w0_tiled + tile_off(un.e, un.nb0, kb), kWTileBytes, full_w(sw), pol_w);
-            if (un.has1)
-              bulk_load(dst + kWTileBytes, a.w1_tiled + tile_off(un.e, un.nb1, kb), kWTileBytes, full_w(sw), pol_w);
+          if (a.w_tiled) {
+            // both weight blocks of the K block are one contiguous 32 KB image
+            mbar_arrive_expect_tx(full_w(sw), 2 * kWTileBytes);
+            bulk_load(dst, a.w_tiled + unit_off(un.e, un.ru, kb), 2 * kWTileBytes, full_w(sw), pol_w);
           } else {
+            mbar_arrive_expect_tx(full_w(sw), (un.has1 ? 2 : 1) * kWTileBytes);
             tma_load_3d(dst, &tm_w0, full_w(sw), kb * 128, un.nb0 * 128, un.e, pol_w);
             if (un.has1) tma_load_3d(dst + kWTileBytes, &tm_w1, full_w(sw), kb * 128, un.nb1 * 128, un.e, pol_w);
           }
@@ -491,8 +492,7 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (fa.numRegs * kThreadsW < 128 * kRegsProducer + 256 * kRegsEpilogue) return cudaErrorInvalidConfiguration;
   WideArgs a;
-  a.w0_tiled = g.w0_tiled;
-  a.w1_tiled = g.w1_tiled;
+  a.w_tiled = g.w_tiled;
   a.s0 = g.s0;
   a.s1 = g.s1;
   a.tiles = g.tiles;
