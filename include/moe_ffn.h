@@ -153,6 +153,11 @@ moe_status moe_permute(const moe_dims *dims, int64_t n_tokens, const int32_t *to
                        int32_t *inv_pos, int32_t validate, void *workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* moe_permute reads and writes only the first moe_permute_workspace_size bytes
+ * of a workspace (the error word and, for large batches, per-chunk counts), so
+ * a routing-only caller may pass a buffer of that size.  0 for unsupported dims. */
+size_t moe_permute_workspace_size(const moe_dims *dims, int64_t n_tokens);
+
 /* Expert pass ("Mixture of experts" page, moe_infer: gather the sorted token
  * rows, run each expert on its slice, write each output row back to its
  * position; "SwiGLU output" / "Element-wise product" pages for the expert).

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_dims), ctypes.c_int64, ctypes.c_int32]),
     "moe_tiled_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "moe_permute_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_dims), ctypes.c_int64]),
     "moe_pack_weights": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(moe_weights),
                                          ctypes.POINTER(moe_weights), ctypes.c_void_p]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 5
@@ -146,6 +147,10 @@ def moe_status_string(status: int) -> str:
 
 def moe_workspace_size(dm: moe_dims, n_tokens: int, d_ff_shared: int = 0) -> int:
     return load_library().moe_workspace_size(ctypes.byref(dm), n_tokens, d_ff_shared)
+
+
+def moe_permute_workspace_size(dm: moe_dims, n_tokens: int) -> int:
+    return load_library().moe_permute_workspace_size(ctypes.byref(dm), n_tokens)
 
 
 def moe_tiled_bytes(which: int, num_experts: int, d: int, d_ff: int) -> int:
@@ -264,7 +269,10 @@ def permute(topk_ids, num_experts: int, ws=None, validate=False, stream=None):
     n, k = topk_ids.shape
     dm = moe_dims(128, 128, num_experts, k)
     if ws is None:
-        ws = torch.zeros(256, dtype=torch.uint8, device=topk_ids.device)
+        nbytes = load_library().moe_permute_workspace_size(ctypes.byref(dm), n)
+        if nbytes == 0:
+            raise MoeError(2, "moe_permute_workspace_size")
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=topk_ids.device)
     dev = topk_ids.device
     counts = torch.empty(num_experts, dtype=torch.int32, device=dev)
     offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)

@@ -22,7 +22,7 @@ constexpr int kMaxTopK = 32;
 // Sorted activations and h are kept in the split format (split3.cuh): e4m3
 // codes [3 rows][width] plus one fp32 exponent factor per (128 columns, row).
 struct Layout {
-  size_t err = 0, n_tiles = 64, tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
+  size_t err = 0, n_tiles = 64, route = 256, route_end = 256, tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
   size_t xs = 0, xs_inv = 0, h = 0, h_inv = 0, xs_sh = 0, xs_sh_inv = 0, h_sh = 0, h_sh_inv = 0, sh_out = 0;
   size_t rows = 0, total = 0;
 };
@@ -37,7 +37,7 @@ bool dims_ok(const moe_dims* d) {
 bool make_layout(const moe_dims* d, int64_t n, int32_t dff_sh, Layout* L) {
   if (!dims_ok(d) || n < 0 || dff_sh < 0 || dff_sh % 128 != 0) return false;
   const int64_t R = n * d->top_k;
-  if (R >= (int64_t(1) << 31)) return false;
+  if (R >= (int64_t(1) << 31) - 4096) return false;
   const int64_t max_tiles = R / kNTokSmall + d->num_experts + 1;  // bound for either tile width
   const int64_t max_tiles_sh = n / kNTokSmall + 2;
   size_t off = 256;
@@ -46,6 +46,9 @@ bool make_layout(const moe_dims* d, int64_t n, int32_t dff_sh, Layout* L) {
     off = align_up(off + bytes);
     return at;
   };
+  // the routing plan's scratch comes first, so moe_permute needs only a short prefix
+  L->route = take(4 * size_t(route_scratch_ints(R, d->num_experts)));
+  L->route_end = off;
   L->tiles = take(sizeof(TileDesc) * max_tiles);
   L->tiles_sh = take(sizeof(TileDesc) * max_tiles_sh);
   L->counts = take(4 * size_t(d->num_experts));
@@ -366,6 +369,12 @@ size_t moe_workspace_size(const moe_dims* dims, int64_t n_tokens, int32_t d_ff_s
   return L.total;
 }
 
+size_t moe_permute_workspace_size(const moe_dims* dims, int64_t n_tokens) {
+  Layout L;
+  if (!make_layout(dims, n_tokens, 0, &L)) return 0;
+  return L.route_end;
+}
+
 size_t moe_tiled_bytes(int32_t which, int32_t E, int32_t d, int32_t dff) {
   if (E < 1 || d <= 0 || dff <= 0 || d % 128 != 0 || dff % 128 != 0) return 0;
   if (which == 0) return static_cast<size_t>(pack_tile_count(E, dff, d, 0)) * 16384;
@@ -407,12 +416,13 @@ moe_status moe_permute(const moe_dims* dims, int64_t n, const int32_t* topk_ids,
   Layout L;
   if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
-  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < L.route_end) return MOE_ERR_WORKSPACE;
   if (!tokens_per_expert || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (n > 0 && (!topk_ids || !sorted_pos)) return MOE_ERR_INVALID_ARG;
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, tokens_per_expert,
-                           expert_offsets, sorted_pos, inv_pos, validate, err, s) != cudaSuccess)
+                           expert_offsets, sorted_pos, inv_pos, validate, at<int32_t>(ws, L.route), err,
+                           s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -465,7 +475,7 @@ moe_status moe_infer(const moe_dims* dims, int64_t n, const void* x, const int32
   int32_t* ip = at<int32_t>(ws, L.inv_pos);
   uint32_t* err = at<uint32_t>(ws, L.err);
   MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
-                                      offsets, sp, ip, 0, err, s));
+                                      offsets, sp, ip, 0, at<int32_t>(ws, L.route), err, s));
   tr.after("route_permute");
   void* rows = at<void>(ws, L.rows);
   moe_status st = experts_pass(dims, n, x, topk_weight, offsets, sp, w, rows, ws, L, true, true, s, tr);
@@ -498,7 +508,7 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
   int32_t* ip = at<int32_t>(ws, L.inv_pos);
   uint32_t* err = at<uint32_t>(ws, L.err);
   MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
-                                      offsets, sp, ip, 0, err, s));
+                                      offsets, sp, ip, 0, at<int32_t>(ws, L.route), err, s));
   tr.after("route_permute");
   const int64_t R = n * dims->top_k;
   MOE_CHECK_CUDA(launch_rmsnorm_scatter(

@@ -14,7 +14,9 @@ pytestmark = pytest.mark.gpu
 
 def _run(ids_host, E, validate=False):
     ids = ids_host.cuda()
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    nbytes = mx.moe_permute_workspace_size(mx.dims(128, 128, E, ids.shape[1]), ids.shape[0])
+    assert nbytes >= 256
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     counts, offsets, sp, ip = mx.permute(ids, E, ws=ws, validate=validate)
     err = mx.moe_get_error(ws)
     return counts.cpu().numpy(), offsets.cpu().numpy(), sp.cpu().numpy(), ip.cpu().numpy(), err
@@ -37,15 +39,17 @@ def test_permute_workloads_bit_exact(name):
     _check(ids, wl.num_experts)
 
 
+# one CTA plans up to 8192 entries; larger batches run in chunks of 2048 entries over many CTAs
 @pytest.mark.parametrize("n,k,E", [(1, 8, 384), (1, 1, 1), (3, 5, 33), (37, 8, 384), (1000, 7, 1024),
-                                   (777, 3, 64), (4097, 8, 384)])
+                                   (777, 3, 64), (1024, 8, 16), (1025, 8, 16), (2049, 5, 1024), (4097, 8, 384)])
 def test_permute_ragged_shapes(n, k, E):
     ids = syn.routing_uniform(n, E, k, torch.Generator().manual_seed(n * 31 + k))
     _check(ids, E)
 
 
-def test_permute_all_tokens_one_expert():
-    ids = torch.full((5000, 1), 17, dtype=torch.int32)
+@pytest.mark.parametrize("n", [5000, 20000])
+def test_permute_all_tokens_one_expert(n):
+    ids = torch.full((n, 1), 17, dtype=torch.int32)
     _check(ids, 384)
 
 
@@ -70,3 +74,20 @@ def test_permute_duplicates_flagged_only_when_validating():
     *_, err = _run(ids, 8, validate=True)
     assert err == 4
     _check(ids, 8)   # histogram semantics: a duplicated id counts twice, as in the oracle
+
+
+def test_permute_errors_in_chunked_plan():
+    # 3000 x 8 entries: the chunked path; bad ids in several chunks, one duplicate
+    g = torch.Generator().manual_seed(11)
+    ids = syn.routing_uniform(3000, 64, 8, g)
+    ids[5, 2] = 64
+    ids[1500, 0] = -3
+    ids[2999, 7] = 1000
+    _check(ids, 64)
+    ids = syn.routing_uniform(3000, 64, 8, g)
+    ids[2100, 3] = ids[2100, 4]
+    *_, err = _run(ids, 64, validate=False)
+    assert err == mx.MOE_OK
+    *_, err = _run(ids, 64, validate=True)
+    assert err == 4
+    _check(ids, 64)
