@@ -20,7 +20,7 @@
 // MMA holds the three terms of NTOK tokens (N = 3 NTOK).  Per 128-wide K block:
 //
 //   warp 0      weight producer: stages of KPS K blocks x both weight blocks
-//               into a ring, L2 prefetch a few stages ahead.
+//               into a ring.
 //   warp 2      activation producer: the block of 3 NTOK rows x 128 bytes
 //               into its own ring, so neither ring throttles the other.
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=3 NTOK, K=32) per
@@ -48,7 +48,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarpProducer = 0;     // weight loads and L2 prefetch
+constexpr int kWarpProducer = 0;     // weight loads
 constexpr int kWarpMma = 1;
 constexpr int kWarpActProducer = 2;  // activation loads
 constexpr int kWarpEpi0 = 4;         // epilogue: warps 4..7 -> tensor-memory lane quarters 0..3
@@ -61,6 +61,7 @@ constexpr int pow2_at_least(int v) {
 
 template <int NTOK, int KPS, int WST, int BST, int DST>
 struct Cfg {
+  static_assert(NTOK <= 32, "one token per lane for the activation exponents");
   static constexpr int kNB = 3 * NTOK;                   // MMA N: three e4m3 terms per token
   static constexpr int kWTile = 128 * 128;               // e4m3 weight tile bytes
   static constexpr int kWKb = 2 * kWTile;                // both weight blocks of one K block
@@ -73,8 +74,6 @@ struct Cfg {
   static constexpr int kBarOffset = kBOffset + BST * kBStage;
   static constexpr int kRedOffset = kBarOffset + kNumBars * 8 + 16;
   static constexpr int kSmem = 1024 + kRedOffset + 2 * 4 * NTOK * 4;
-  // L2 prefetch runs this many weight stages ahead of the loads (about 128 KB).
-  static constexpr int kPrefetch = (128 * 1024) / kWStage;
   static_assert(kBStage % 1024 == 0, "activation stages must stay 1024-byte aligned");
   static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
   static_assert(kNB % 16 == 0 && kNB <= 256, "MMA N for M = 128");
@@ -201,28 +200,9 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   if (warp == kWarpProducer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      // L2 prefetch cursor, kPrefetch stages ahead of the loads
-      int pf_u = blockIdx.x, pf_kb = 0;
-      Unit16 pf{};
-      auto prefetch_one = [&]() {
-        if (pf_u >= total_units) return;
-        if (pf_kb == 0) pf = unit16(a, a.tiles[pf_u / upt], pf_u, upt);
-        const int nk = min(KPS, num_kb - pf_kb);
-        if (a.w_tiled) {
-          bulk_prefetch_l2(a.w_tiled + unit_off(pf.e, pf.ru, pf_kb), nk * C::kWKb);
-        } else {
-          for (int j = 0; j < nk; ++j) {
-            tma_prefetch_3d(&tm_w0, (pf_kb + j) * 128, pf.nb0 * 128, pf.e);
-            if (pf.has1) tma_prefetch_3d(&tm_w1, (pf_kb + j) * 128, pf.nb1 * 128, pf.e);
-          }
-        }
-        pf_kb += nk;
-        if (pf_kb == num_kb) {
-          pf_kb = 0;
-          pf_u += gridDim.x;
-        }
-      };
-      for (int i = 0; i < C::kPrefetch; ++i) prefetch_one();
+      // No L2 prefetch ahead of the stages: with six 32-64 KB stages per SM in
+      // flight the stream already saturates HBM, and extra prefetch requests
+      // measured 5-7 % slower.
       uint32_t w_issued = 0;  // weight stages issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
@@ -251,7 +231,6 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             }
           }
           ++w_issued;
-          prefetch_one();
         }
       }
       if (!ok)  // wait for the copies already in flight before the CTA exits
@@ -299,6 +278,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             break;
           }
           const uint32_t wst = sbase + sw * C::kWStage;
+          const uint64_t wdesc = desc_kmajor_sw128(wst);
           for (int j = 0; j < nk; ++j, ++it) {
             const int sb = it % BST, sd = it % DST;
             if (!wait_bounded(full_b(sb), (it / BST) & 1, abort_flag, a.err) ||
@@ -307,15 +287,15 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
               break;
             }
             tc_fence_after();
-            const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
+            const uint64_t bdesc = desc_kmajor_sw128(sbase + C::kBOffset + sb * C::kBStage);
+            const uint64_t wj = desc_advance(wdesc, j * C::kWKb);
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               if (m == 1 && !has1) break;
               const uint32_t d_addr = tmem + (sd * 2 + m) * NB;
-              const uint32_t wtile = wst + j * C::kWKb + m * C::kWTile;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ss(d_addr, desc_kmajor_sw128(wtile + kk * 32), desc_kmajor_sw128(bst + kk * 32), idesc,
+                mma_f8_ss(d_addr, desc_advance(wj, m * C::kWTile + kk * 32), desc_advance(bdesc, kk * 32), idesc,
                           kk > 0 ? 1u : 0u);
             }
             tc_commit(empty_b(sb));
@@ -358,19 +338,20 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         for (int j = 0; j < NTOK; ++j)
           wgt[j] = (j < td.n_valid && a.topk_weight) ? __ldg(a.topk_weight + dest[j]) : 1.0f;
       }
-      // scales of the first K block; each iteration loads the next block's
+      // Per K block: the two blocks' weight scales and, in lane j, the 2^-s of token j's
+      // activation block ([kb][row]); each iteration loads the next block's, so the
+      // latency hides behind the wait, and the lanes' values reach all lanes by shuffle.
+      const float* inv0 = a.act_inv + td.row_start;
+      const bool tok_lane = lane < NTOK && lane < td.n_valid;
       float s0n = __ldg(sc0), s1n = __ldg(sc1);
+      float sxn = tok_lane ? __ldg(inv0 + lane) : 0.f;
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int sd = it % DST;
-        const float s0v = s0n, s1v = s1n;
-        // 2^-s of each token's activation block, [kb][row]; the next block's line is
-        // pulled into L1 now so the reads after the wait below hit
-        const float* inv = a.act_inv + static_cast<int64_t>(kb) * a.act_rows + td.row_start;
+        const float s0v = s0n, s1v = s1n, sx_lane = sxn;
         if (kb + 1 < num_kb) {
           s0n = __ldg(sc0 + kb + 1);
           s1n = __ldg(sc1 + kb + 1);
-          if (lane < (NTOK + 31) / 32 + 1 && td.row_start + lane * 32 < a.act_rows)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(inv + a.act_rows + lane * 32) : "memory");
+          sxn = tok_lane ? __ldg(inv0 + static_cast<int64_t>(kb + 1) * a.act_rows + lane) : 0.f;
         }
         ok = __all_sync(0xffffffffu, wait_bounded(dfull(sd), (it / DST) & 1, abort_flag, a.err));
         if (!ok) break;
@@ -379,7 +360,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         for (int c = 0; c < NTOK / 16; ++c) {  // 16 tokens (48 tensor-memory columns) at a time
           float sx[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sx[j] = 16 * c + j < td.n_valid ? __ldg(inv + 16 * c + j) : 0.f;
+          for (int j = 0; j < 16; ++j) sx[j] = __shfl_sync(0xffffffffu, sx_lane, 16 * c + j);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             if (m == 1 && !un.has1) break;

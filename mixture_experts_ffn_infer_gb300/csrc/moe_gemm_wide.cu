@@ -324,15 +324,15 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
             break;
           }
           tc_fence_after();
-          const uint32_t wst = sbase + sw * C::kWStage;
-          const uint32_t ast = sbase + C::kAOff + sa * C::kAStage;
+          const uint64_t wdesc = desc_kmajor_sw128(sbase + sw * C::kWStage);
+          const uint64_t adesc = desc_kmajor_sw128(sbase + C::kAOff + sa * C::kAStage);
           const uint32_t d = tmem + static_cast<uint32_t>(sd) * 256;
 #pragma unroll
           for (int t = TX - 1; t >= 0; --t) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f8(d, desc_kmajor_sw128(ast + t * (kTileMax * 128) + kk * 32), desc_kmajor_sw128(wst + kk * 32),
-                     idesc, (t < TX - 1 || kk > 0) ? 1u : 0u);
+              mma_f8(d, desc_advance(adesc, t * (kTileMax * 128) + kk * 32), desc_advance(wdesc, kk * 32), idesc,
+                     (t < TX - 1 || kk > 0) ? 1u : 0u);
           }
           tc_commit(empty_w(sw));
           tc_commit(empty_a(sa));

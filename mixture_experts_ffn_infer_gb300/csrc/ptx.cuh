@@ -144,6 +144,12 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// The descriptor of saddr + bytes, from that of saddr: the start address sits in
+// the low 14 bits in 16-byte units and shared-memory addresses stay below
+// 256 KB, so the offset adds without a carry.  Cheaper in an MMA issue loop
+// than building each descriptor.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // 32 lanes x 32 bit, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
