@@ -276,11 +276,11 @@ moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t exper
 // `gather` selects the bf16 row gather (moe_experts_forward / moe_infer); the
 // fused layer writes the sorted rows itself (RMSNorm scatter).  Either way the
 // rows are bf16 values, which two e4m3 terms hold.
-// inv_ready: the workspace's inv_pos already holds the inverse of sorted_pos
-// (written by the routing kernel); otherwise the gather derives it first.
+// plan_ready: the routing kernel has already written the workspace's inv_pos (the
+// inverse of sorted_pos) and tile list; otherwise they are derived here first.
 moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float* topk_weight,
                         const int32_t* offsets, const int32_t* sorted_pos, const moe_weights* w, void* rows,
-                        void* ws, const Layout& L, bool gather, bool inv_ready, cudaStream_t s, Tracer& tr) {
+                        void* ws, const Layout& L, bool gather, bool plan_ready, cudaStream_t s, Tracer& tr) {
   const int32_t R = static_cast<int32_t>(n * d->top_k);
   uint8_t* xs = at<uint8_t>(ws, L.xs);
   float* xs_inv = at<float>(ws, L.xs_inv);
@@ -289,13 +289,15 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
   const int x_terms = 2;
   if (gather) {
     int32_t* ip = at<int32_t>(ws, L.inv_pos);
-    if (!inv_ready) MOE_CHECK_CUDA(launch_invert_positions(sorted_pos, R, ip, s));
+    if (!plan_ready) MOE_CHECK_CUDA(launch_invert_positions(sorted_pos, R, ip, s));
     MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), ip, static_cast<int32_t>(n), d->top_k, d->d,
                                       xs, rows_layout(R, d->num_experts, d->d, x_terms), xs_inv, s));
     tr.after("gather_rows");
   }
-  MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
-  tr.after("build_tiles");
+  if (!plan_ready) {
+    MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
+    tr.after("build_tiles");
+  }
   return run_gemms(w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
                    at<float>(ws, L.h_inv), tiles, n_tiles, sorted_pos, topk_weight, rows, at<uint32_t>(ws, L.err), s,
                    tr, "gateup_swiglu", "down_scatter");
@@ -421,8 +423,8 @@ moe_status moe_permute(const moe_dims* dims, int64_t n, const int32_t* topk_ids,
   if (n > 0 && (!topk_ids || !sorted_pos)) return MOE_ERR_INVALID_ARG;
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, tokens_per_expert,
-                           expert_offsets, sorted_pos, inv_pos, validate, at<int32_t>(ws, L.route), err,
-                           s) != cudaSuccess)
+                           expert_offsets, sorted_pos, inv_pos, validate, at<int32_t>(ws, L.route), err, 0, nullptr,
+                           nullptr, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -475,7 +477,9 @@ moe_status moe_infer(const moe_dims* dims, int64_t n, const void* x, const int32
   int32_t* ip = at<int32_t>(ws, L.inv_pos);
   uint32_t* err = at<uint32_t>(ws, L.err);
   MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
-                                      offsets, sp, ip, 0, at<int32_t>(ws, L.route), err, s));
+                                      offsets, sp, ip, 0, at<int32_t>(ws, L.route), err,
+                                      tile_tokens(n * dims->top_k, dims->num_experts), at<TileDesc>(ws, L.tiles),
+                                      at<int32_t>(ws, L.n_tiles), s));
   tr.after("route_permute");
   void* rows = at<void>(ws, L.rows);
   moe_status st = experts_pass(dims, n, x, topk_weight, offsets, sp, w, rows, ws, L, true, true, s, tr);
@@ -508,7 +512,9 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
   int32_t* ip = at<int32_t>(ws, L.inv_pos);
   uint32_t* err = at<uint32_t>(ws, L.err);
   MOE_CHECK_CUDA(launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, counts,
-                                      offsets, sp, ip, 0, at<int32_t>(ws, L.route), err, s));
+                                      offsets, sp, ip, 0, at<int32_t>(ws, L.route), err,
+                                      tile_tokens(n * dims->top_k, dims->num_experts), at<TileDesc>(ws, L.tiles),
+                                      at<int32_t>(ws, L.n_tiles), s));
   tr.after("route_permute");
   const int64_t R = n * dims->top_k;
   MOE_CHECK_CUDA(launch_rmsnorm_scatter(

@@ -78,10 +78,12 @@ inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms) {
 // ---------------------------------------------------------------- launchers
 // routing.cu
 // scratch: route_scratch_ints(n k, E) ints (none for small batches, which one CTA plans).
+// tiles / n_tiles non-null: also cut the GEMM tile plan of ntok-row tiles from the offsets.
 int64_t route_scratch_ints(int64_t R, int32_t E);
 cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32_t E, int32_t* counts,
                                  int32_t* offsets, int32_t* sorted_pos, int32_t* inv_pos, int32_t validate,
-                                 int32_t* scratch, uint32_t* err, cudaStream_t s);
+                                 int32_t* scratch, uint32_t* err, int32_t ntok, TileDesc* tiles, int32_t* n_tiles,
+                                 cudaStream_t s);
 cudaError_t launch_build_tiles(const int32_t* offsets, int32_t E, int32_t ntok, TileDesc* tiles,
                                int32_t* n_tiles, cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(uint32_t* err, cudaStream_t s);

@@ -60,10 +60,29 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return before + x - v;
 }
 
+// Tiles of at most ntok rows over every expert's slice [offsets[e], offsets[e+1]),
+// in expert order; the whole CTA (kThreads threads) takes part.
+__device__ void cta_build_tiles(const int32_t* __restrict__ offsets, int E, int ntok, TileDesc* __restrict__ tiles,
+                                int32_t* __restrict__ n_tiles, int* warp_sums) {
+  const int tid = threadIdx.x;
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
+  int local = 0;
+  for (int e = e0; e < e1; ++e) local += (offsets[e + 1] - offsets[e] + ntok - 1) / ntok;
+  int total;
+  int t = block_exclusive_scan(local, warp_sums, &total);
+  for (int e = e0; e < e1; ++e) {
+    const int beg = offsets[e], end = offsets[e + 1];
+    for (int r = beg; r < end; r += ntok) tiles[t++] = TileDesc{e, r, min(ntok, end - r), 0};
+  }
+  if (tid == 0) *n_tiles = total;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 route_permute_kernel(const int32_t* __restrict__ ids, int32_t n, int32_t k, int32_t E, int32_t* __restrict__ counts,
                      int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pos, int32_t* __restrict__ inv_pos,
-                     int32_t validate, int32_t reset_err, uint32_t* err) {
+                     int32_t validate, int32_t reset_err, uint32_t* err, int32_t ntok, TileDesc* __restrict__ tiles,
+                     int32_t* __restrict__ n_tiles) {
   extern __shared__ int32_t smem[];
   int32_t* wcnt = smem;                  // [kWarps][E]: counts, then running positions
   int32_t* warp_sums = smem + kWarps * E;  // [32]
@@ -141,6 +160,10 @@ route_permute_kernel(const int32_t* __restrict__ ids, int32_t n, int32_t k, int3
     __syncwarp();
   }
   for (int i = total + tid; i < R; i += kThreads) sorted_pos[i] = -1;
+  if (tiles) {  // the GEMMs' tile plan from the offsets this CTA wrote
+    __syncthreads();
+    cta_build_tiles(offsets, E, ntok, tiles, n_tiles, warp_sums);
+  }
 }
 
 // ------------------------------------------------------------ many CTAs
@@ -196,7 +219,9 @@ __global__ void __launch_bounds__(kChunkThreads) route_count_kernel(const int32_
 // starting position per expert (written over its count).
 __global__ void __launch_bounds__(kThreads, 1) route_scan_kernel(int32_t* __restrict__ chunk_counts, int32_t chunks,
                                                                  int32_t E, int32_t* __restrict__ counts,
-                                                                 int32_t* __restrict__ offsets) {
+                                                                 int32_t* __restrict__ offsets, int32_t ntok,
+                                                                 TileDesc* __restrict__ tiles,
+                                                                 int32_t* __restrict__ n_tiles) {
   __shared__ int warp_sums[32];
   const int tid = threadIdx.x;
   const int per = (E + kThreads - 1) / kThreads;
@@ -220,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) route_scan_kernel(int32_t* __rest
     }
   }
   if (tid == 0) offsets[E] = total;
+  if (tiles) {
+    __syncthreads();
+    cta_build_tiles(offsets, E, ntok, tiles, n_tiles, warp_sums);
+  }
 }
 
 __global__ void __launch_bounds__(kChunkThreads) route_scatter_kernel(const int32_t* __restrict__ ids, int32_t n,
@@ -272,18 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 build_tiles_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t ntok, TileDesc* __restrict__ tiles,
                    int32_t* __restrict__ n_tiles) {
   __shared__ int warp_sums[32];
-  const int tid = threadIdx.x;
-  const int per = (E + kThreads - 1) / kThreads;
-  const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
-  int local = 0;
-  for (int e = e0; e < e1; ++e) local += (offsets[e + 1] - offsets[e] + ntok - 1) / ntok;
-  int total;
-  int t = block_exclusive_scan(local, warp_sums, &total);
-  for (int e = e0; e < e1; ++e) {
-    const int beg = offsets[e], end = offsets[e + 1];
-    for (int r = beg; r < end; r += ntok) tiles[t++] = TileDesc{e, r, min(ntok, end - r), 0};
-  }
-  if (tid == 0) *n_tiles = total;
+  cta_build_tiles(offsets, E, ntok, tiles, n_tiles, warp_sums);
 }
 
 __global__ void identity_tiles_kernel(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles) {
@@ -318,7 +336,8 @@ int64_t route_scratch_ints(int64_t R, int32_t E) {
 
 cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32_t E, int32_t* counts,
                                  int32_t* offsets, int32_t* sorted_pos, int32_t* inv_pos, int32_t validate,
-                                 int32_t* scratch, uint32_t* err, cudaStream_t s) {
+                                 int32_t* scratch, uint32_t* err, int32_t ntok, TileDesc* tiles, int32_t* n_tiles,
+                                 cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   const int64_t R = static_cast<int64_t>(n) * k;
   if (R <= kSingleCtaEntries) {
@@ -327,7 +346,7 @@ cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     route_permute_kernel<<<1, kThreads, smem, s>>>(ids, n, k, E, counts, offsets, sorted_pos, inv_pos, validate, 1,
-                                                   err);
+                                                   err, ntok, tiles, n_tiles);
     return cudaGetLastError();
   }
   if (!scratch) return cudaErrorInvalidValue;
@@ -337,7 +356,7 @@ cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32
   if (e != cudaSuccess) return e;
   route_count_kernel<<<chunks, kChunkThreads, smem, s>>>(ids, n, k, E, validate, scratch, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  route_scan_kernel<<<1, kThreads, 0, s>>>(scratch, chunks, E, counts, offsets);
+  route_scan_kernel<<<1, kThreads, 0, s>>>(scratch, chunks, E, counts, offsets, ntok, tiles, n_tiles);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   route_scatter_kernel<<<chunks, kChunkThreads, smem, s>>>(ids, n, k, E, scratch, offsets, sorted_pos, inv_pos);
   return cudaGetLastError();
