@@ -88,3 +88,33 @@ def test_host_argument_errors_return_codes_without_a_device(lib):
                                0, None, 0, ctypes.c_void_p(addr), 1 << 30, None, None) == 1
     assert L.moe_combine(ctypes.byref(dm), 8, None, None, None, None, 0, None) == 1
     assert L.moe_get_error(None, None) == 1
+
+
+def test_tiled_bytes_and_permute_workspace(lib):
+    # gate and up interleaved: twice one matrix; down in row-block pairs, padded to an even count
+    assert mx.moe_tiled_bytes(0, 384, 7168, 2048) == 2 * 384 * 2048 * 7168
+    assert mx.moe_tiled_bytes(2, 384, 7168, 2048) == 384 * 7168 * 2048
+    assert mx.moe_tiled_bytes(2, 3, 384, 256) == 3 * 4 * 128 * 256          # 3 row blocks -> 2 pairs
+    assert mx.moe_tiled_bytes(1, 3, 384, 256) == 0                          # w_up is not a tiled buffer
+    assert mx.moe_tiled_bytes(0, 3, 300, 256) == 0                          # d not a multiple of 128
+    # the routing prefix of the workspace: the error word only for small batches,
+    # plus per-chunk counts above 8192 entries, and never more than the whole workspace
+    dm = mx.dims(7168, 2048, 384, 8)
+    small = mx.moe_permute_workspace_size(dm, 16)
+    large = mx.moe_permute_workspace_size(dm, 32768)
+    assert 256 <= small <= 4096
+    assert large >= small + (32768 * 8 // 2048) * 384 * 4
+    assert large < mx.moe_workspace_size(dm, 32768)
+    assert mx.moe_permute_workspace_size(mx.dims(7168, 2048, 2000, 8), 16) == 0
+
+
+def test_permute_rejects_a_workspace_shorter_than_its_prefix(lib):
+    dm = mx.dims(128, 128, 384, 8)
+    n = 4096                                   # 32768 entries: the chunked plan needs scratch
+    need = mx.moe_permute_workspace_size(dm, n)
+    buf = (ctypes.c_uint8 * (need + 256))()
+    addr = (ctypes.addressof(buf) + 255) & ~255
+    dummy = ctypes.c_void_p(addr)
+    st = lib.moe_permute(ctypes.byref(dm), n, dummy, dummy, dummy, dummy, None, 0, ctypes.c_void_p(addr), need - 1,
+                         None)
+    assert st == 3
