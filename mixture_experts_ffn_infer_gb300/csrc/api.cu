@@ -20,7 +20,9 @@ constexpr int kMaxTopK = 32;
 
 // ---------------------------------------------------------------- workspace
 // Sorted activations and h are kept in the split format (split3.cuh): e4m3
-// codes [3 rows][width] plus one fp32 exponent factor per (128 columns, row).
+// codes (rows interleaved with their three terms for 16-token tiles, one plane
+// per term for wide tiles; SplitLayout) plus one fp32 exponent factor per
+// (128 columns, row).
 struct Layout {
   size_t err = 0, n_tiles = 64, route = 256, route_end = 256, tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
   size_t xs = 0, xs_inv = 0, h = 0, h_inv = 0, xs_sh = 0, xs_sh_inv = 0, h_sh = 0, h_sh_inv = 0, sh_out = 0;

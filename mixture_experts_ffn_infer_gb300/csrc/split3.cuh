@@ -1,4 +1,4 @@
-// Activations as three e4m3 terms with a power-of-two scale per 128-column block.
+// Activations as two or three e4m3 terms with a power-of-two scale per 128-column block.
 //
 // The expert GEMMs run on the tensor core's e4m3 x e4m3 path so the FP8
 // weights feed the MMA unconverted.  An activation value v of a 128-element
@@ -7,9 +7,10 @@
 // a1 = e4m3(v * 2^s), a2 = e4m3(remainder), a3 = e4m3(next remainder), each
 // rounded to nearest.  Each term carries 4 significant bits, so a bf16 value
 // (8 bits) is reproduced exactly by the first two terms whenever the block's
-// range stays inside e4m3's; the third term carries an fp32 intermediate to
-// about 12 bits.  The GEMM sums the three partial products and multiplies by
-// 2^-s in fp32.
+// range stays inside e4m3's (so bf16 rows are stored as two terms); the third
+// term carries an fp32 intermediate (h) to about 12 bits.  The GEMMs sum the
+// terms' partial products - in the epilogue for 16-token tiles, in the tensor
+// core's accumulator for wide tiles - and multiply by 2^-s in fp32.
 #pragma once
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
