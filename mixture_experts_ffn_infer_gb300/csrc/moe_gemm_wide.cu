@@ -40,7 +40,7 @@
 //
 // At the end of a unit the gate/up epilogue forms h = silu(g) * u and writes
 // it as three term planes, one exponent per (token, 128 features) from the
-// maximum over both feature halves; the down epilogue writes
+// maximum over both feature halves (their float exponents, exchanged as bytes); the down epilogue writes
 // f16(topk_weight * o) to the row's flat position.  Every wait is bounded; a
 // wait that gives up raises the abort flag and the device error word, and
 // every role drains what it has in flight before the kernel returns.
@@ -67,8 +67,8 @@ struct WideCfg {
   static constexpr int kWStage = 2 * kWTileBytes;          // both weight blocks of one K block
   static constexpr int kAStage = TX * kTileMax * 128;      // the activation box: terms x 128 rows
   static constexpr int kAOff = WST * kWStage;
-  static constexpr int kRedOff = kAOff + AST * kAStage;    // h block maxima [parity][half][128 tokens]
-  static constexpr int kRedBytes = 2 * 2 * kTileMax * 4;
+  static constexpr int kRedOff = kAOff + AST * kAStage;    // h block-maximum exponents [parity][half][128 tokens]
+  static constexpr int kRedBytes = 2 * 2 * kTileMax;
   static constexpr int kBarOff = kRedOff + kRedBytes;
   static constexpr int kNumBars = 2 * WST + 2 * AST + 2 * 2 + 2 + 1;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
@@ -191,7 +191,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
   const uint32_t drain_bar = bar0 + 8u * (C::kNumBars - 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + C::kNumBars * 8);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  float* red = reinterpret_cast<float*>(smem + C::kRedOff);
+  uint8_t* red = smem + C::kRedOff;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -424,14 +424,18 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           overflow |= !(fabsf(acc0[j]) <= 3.0e38f);
         }
         overflow &= valid;
-        float* rb = red + (ui & 1) * 2 * kTileMax;
-        rb[hf * kTileMax + tok] = m;
+        // the biased float exponent of the maximum is all the block scale needs
+        uint8_t* rb = red + (ui & 1) * 2 * kTileMax;
+        const uint32_t code = __float_as_uint(m) >> 23;  // m >= 0: 0 for zero or subnormal, 255 for inf
+        rb[hf * kTileMax + tok] = static_cast<uint8_t>(code);
         __syncwarp();
         if (lane == 0) mbar_arrive(redbar(ui & 1));
         ok = __all_sync(0xffffffffu, wait_bounded(redbar(ui & 1), (ui >> 1) & 1, abort_flag, a.err));
         if (!ok) break;
         if (valid) {
-          const int sexp = split_exponent(fmaxf(m, rb[(hf ^ 1) * kTileMax + tok]));
+          // s = 8 - frexp exponent of the larger maximum (split_exponent), from the codes
+          const uint32_t c = max(code, static_cast<uint32_t>(rb[(hf ^ 1) * kTileMax + tok]));
+          const int sexp = (c == 0u || c == 255u) ? 0 : 134 - static_cast<int>(c);
           const float f1 = pow2i(sexp >> 1), f2 = pow2i(sexp - (sexp >> 1));  // both factors stay normal
           const int64_t ld = static_cast<int64_t>(n_nb) * 128;
           uint8_t* hp = static_cast<uint8_t*>(a.out) + row * ld + un.nb0 * 128 + hf * kHalfF;
