@@ -45,6 +45,9 @@ def test_tiny_infer_bf16_and_fp32_outputs():
     (64, 128, 128, 1, 1, 5),       # single expert
     (600, 256, 256, 2, 1, 6),      # 300 rows per expert: tiles of 128, 128 and 44 rows
     (150, 1152, 256, 4, 2, 8),     # nine 128-row blocks of down: the last pair has one block
+    (40, 256, 128, 64, 32, 12),    # the largest top-k (32): 1280 rows over 64 experts
+    (24, 128, 256, 1024, 4, 13),   # the largest expert count (1024), almost every expert empty
+    (200, 256, 128, 40, 32, 14),   # top-k 32 with 160 rows per expert: wide tiles
 ])
 def test_small_shapes_infer(n, d, dff, E, k, seed):
     wl = syn.Workload("s", n, d, dff, E, k, seed=seed)
