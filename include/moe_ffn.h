@@ -107,6 +107,9 @@ typedef struct {
     int32_t n_events;                   /* in: events usable */
     int32_t n_recorded;                 /* out */
     const char *labels[MOE_TRACE_MAX];  /* out */
+    int32_t gemms_only;                 /* in: nonzero = events only around the grouped GEMMs:
+                                           events[0] just before the first, events[i + 1] after the i-th */
+    int32_t n_launched;                 /* out: kernels the call launched */
 } moe_trace;
 
 /* Bytes of workspace that every call below needs for n tokens (d_ff_shared =

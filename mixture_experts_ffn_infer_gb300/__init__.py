@@ -51,7 +51,8 @@ class moe_weights(ctypes.Structure):
 
 class moe_trace(ctypes.Structure):
     _fields_ = [("events", ctypes.c_void_p * MOE_TRACE_MAX), ("n_events", ctypes.c_int32),
-                ("n_recorded", ctypes.c_int32), ("labels", ctypes.c_char_p * MOE_TRACE_MAX)]
+                ("n_recorded", ctypes.c_int32), ("labels", ctypes.c_char_p * MOE_TRACE_MAX),
+                ("gemms_only", ctypes.c_int32), ("n_launched", ctypes.c_int32)]
 
 
 _lib = None

@@ -160,6 +160,9 @@ int num_sms() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Kernels the routing plan launches for R flattened entries (one CTA, or count + scan + scatter).
+int route_kernels(int64_t R) { return route_scratch_ints(R, 1) > 0 ? 3 : 1; }
+
 bool weights_ok(const moe_weights* w) {
   if (!w || !w->w_gate || !w->w_down || !w->s_gate || !w->s_up || !w->s_down || !aligned(w->w_gate, 16) ||
       !aligned(w->w_down, 16))
@@ -176,16 +179,27 @@ bool map_bank(const moe_weights* w, int64_t d, int64_t dff, int64_t E, CUtensorM
          map_weights(dn, w->w_down, dff, d, E);
 }
 
+// Per-kernel events for timing (moe_trace).  Every event sits between two
+// kernels and costs the stream about a launch gap, so gemms_only keeps three
+// per step: before the first GEMM and after each.
 struct Tracer {
   moe_trace* t;
   cudaStream_t s;
   void begin() {
     if (!t) return;
     t->n_recorded = 0;
+    t->n_launched = 0;
+    if (t->gemms_only) return;
     if (t->n_events > 0 && cudaEventRecord(t->events[0], s) == cudaSuccess) t->n_recorded = 1;
   }
-  void after(const char* label) {
-    if (!t || t->n_recorded < 1) return;
+  void before_gemm() {
+    if (!t || !t->gemms_only || t->n_recorded > 0) return;
+    if (t->n_events > 0 && cudaEventRecord(t->events[0], s) == cudaSuccess) t->n_recorded = 1;
+  }
+  // after each launch step; `kernels` is how many kernels that step launched
+  void after(const char* label, bool gemm = false, int kernels = 1) {
+    if (t) t->n_launched += kernels;
+    if (!t || t->n_recorded < 1 || (t->gemms_only && !gemm)) return;
     const int i = t->n_recorded;
     if (i >= t->n_events || i >= MOE_TRACE_MAX) return;
     t->labels[i - 1] = label;
@@ -219,7 +233,8 @@ struct ActMaps {
 // the layout rows_layout gives, x_terms terms), tiles cut at tile_tokens(rows,
 // experts) rows.  Down writes f16(topk_weight * o) to out[sorted_pos[row]]
 // (identity and weight 1 when those are null).
-moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t experts, int32_t rows, int x_terms,
+moe_status run_gemms(bool after_gather, const moe_weights* w, int64_t d, int64_t dff, int64_t experts,
+                     int32_t rows, int x_terms,
                      uint8_t* xs, float* xs_inv, uint8_t* h, float* h_inv, TileDesc* tiles, int32_t* n_tiles,
                      const int32_t* sorted_pos, const float* topk_weight, void* out, uint32_t* err, cudaStream_t s,
                      Tracer& tr, const char* label_gateup, const char* label_down) {
@@ -250,11 +265,14 @@ moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t exper
   g.out_inv = h_inv;
   g.err = err;
   g.num_sms = num_sms();
+  g.overlap = after_gather;
   if (g.num_sms <= 0) return MOE_ERR_CUDA;
+  tr.before_gemm();
   MOE_CHECK_CUDA(launch_gateup(g, s));
-  tr.after(label_gateup);
+  tr.after(label_gateup, true);
 
   GemmLaunch q = g;
+  q.overlap = false;
   q.terms = 3;
   q.w0 = &m_d;
   q.w1 = &m_d;
@@ -270,7 +288,7 @@ moe_status run_gemms(const moe_weights* w, int64_t d, int64_t dff, int64_t exper
   q.sorted_pos = sorted_pos;
   q.topk_weight = topk_weight;
   MOE_CHECK_CUDA(launch_down(q, s));
-  tr.after(label_down);
+  tr.after(label_down, true);
   return MOE_OK;
 }
 
@@ -300,7 +318,7 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
     MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
     tr.after("build_tiles");
   }
-  return run_gemms(w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
+  return run_gemms(gather, w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
                    at<float>(ws, L.h_inv), tiles, n_tiles, sorted_pos, topk_weight, rows, at<uint32_t>(ws, L.err), s,
                    tr, "gateup_swiglu", "down_scatter");
 }
@@ -312,7 +330,7 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
   MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), tile_tokens(n, 1), tiles, n_tiles, s));
   tr.after("shared_tiles");
-  return run_gemms(w, d->d, dff_sh, 1, static_cast<int32_t>(n), 2, at<uint8_t>(ws, L.xs_sh),
+  return run_gemms(false, w, d->d, dff_sh, 1, static_cast<int32_t>(n), 2, at<uint8_t>(ws, L.xs_sh),
                    at<float>(ws, L.xs_sh_inv), at<uint8_t>(ws, L.h_sh), at<float>(ws, L.h_sh_inv), tiles, n_tiles,
                    nullptr, nullptr, at<uint16_t>(ws, L.sh_out), at<uint32_t>(ws, L.err), s, tr, "shared_gateup",
                    "shared_down");
@@ -482,7 +500,7 @@ moe_status moe_infer(const moe_dims* dims, int64_t n, const void* x, const int32
                                       offsets, sp, ip, 0, at<int32_t>(ws, L.route), err,
                                       tile_tokens(n * dims->top_k, dims->num_experts), at<TileDesc>(ws, L.tiles),
                                       at<int32_t>(ws, L.n_tiles), s));
-  tr.after("route_permute");
+  tr.after("route_permute", false, route_kernels(n * dims->top_k));
   void* rows = at<void>(ws, L.rows);
   moe_status st = experts_pass(dims, n, x, topk_weight, offsets, sp, w, rows, ws, L, true, true, s, tr);
   if (st != MOE_OK) return st;
@@ -517,7 +535,7 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
                                       offsets, sp, ip, 0, at<int32_t>(ws, L.route), err,
                                       tile_tokens(n * dims->top_k, dims->num_experts), at<TileDesc>(ws, L.tiles),
                                       at<int32_t>(ws, L.n_tiles), s));
-  tr.after("route_permute");
+  tr.after("route_permute", false, route_kernels(n * dims->top_k));
   const int64_t R = n * dims->top_k;
   MOE_CHECK_CUDA(launch_rmsnorm_scatter(
       static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain), eps, static_cast<int32_t>(n), dims->d,

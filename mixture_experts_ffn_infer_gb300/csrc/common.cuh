@@ -75,6 +75,25 @@ inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms) {
   return wide ? SplitLayout{K, rows * K, terms} : SplitLayout{3 * K, K, 3};
 }
 
+// Launch with programmatic stream serialization when `overlap`: the kernel may
+// start while the previous kernel in the stream finishes (it calls pdl_wait
+// before it reads that kernel's results).
+template <typename... P, typename... A>
+cudaError_t launch_maybe_overlapped(void (*kern)(P...), int grid, int block, size_t smem, cudaStream_t s,
+                                    bool overlap, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
+
 // ---------------------------------------------------------------- launchers
 // routing.cu
 // scratch: route_scratch_ints(n k, E) ints (none for small batches, which one CTA plans).
@@ -136,6 +155,7 @@ struct GemmLaunch {
   const float* topk_weight;     // down: flat router weights (NULL = 1)
   uint32_t* err;
   int num_sms;
+  bool overlap;                 // gate/up: launched behind the row gather (dependent launch)
 };
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s);

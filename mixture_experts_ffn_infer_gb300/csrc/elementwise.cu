@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
                                                                   const int32_t* __restrict__ inv_pos, int32_t n,
                                                                   int32_t k, int32_t d, uint8_t* __restrict__ xs,
                                                                   SplitLayout lay, float* __restrict__ xs_inv) {
+  // the gate/up GEMM may start streaming its weights now; it waits for these rows
+  pdl_launch_dependents();
   const int64_t t = blockIdx.x;
   const int64_t R = static_cast<int64_t>(n) * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -239,6 +239,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     }
     __syncwarp();
   } else if (warp == kWarpActProducer) {
+    pdl_wait();  // the activations are the previous kernel's output
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();
       uint32_t b_issued = 0;
@@ -309,6 +310,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     }
     __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+    pdl_wait();  // activation exponents come from the previous kernel
     const int q = warp - kWarpEpi0;
     const int r = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -470,8 +472,10 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;
-  kern<<<g.num_sms, kThreads, C::kSmem, s>>>(*g.w0, *g.w1, *g.act, a);
-  return cudaGetLastError();
+  // gate/up after the row gather: its CTAs fit beside the gather's, so they start
+  // streaming weights at once (the gather triggers its dependents on entry)
+  return launch_maybe_overlapped(kern, g.num_sms, kThreads, C::kSmem, s, GATEUP && g.overlap, *g.w0, *g.w1,
+                                 *g.act, a);
 }
 
 }  // namespace

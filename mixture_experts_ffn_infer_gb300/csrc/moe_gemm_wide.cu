@@ -286,6 +286,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
     }
     __syncwarp();
   } else if (warp == kWarpAct) {
+    pdl_wait();  // the activations are the previous kernel's output
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();
       uint32_t ai = 0;
@@ -345,6 +346,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
     __syncwarp();
   } else if (warp >= kWarpEpi) {
     regs_inc_epilogue();
+    pdl_wait();  // activation exponents come from the previous kernel
     const int q = warp & 3;                  // tensor-memory lane quarter: tokens 32q..32q+31
     const int hf = (warp - kWarpEpi) >> 2;   // feature half of each weight block
     const int tok = q * 32 + lane;           // this thread's token within the tile
@@ -512,8 +514,9 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;
-  kern<<<g.num_sms, kThreadsW, C::kSmem, s>>>(*g.w0, *g.w1, *g.act_box, a);
-  return cudaGetLastError();
+  // gate/up behind the row gather starts streaming weights on any SM with room
+  return launch_maybe_overlapped(kern, g.num_sms, kThreadsW, C::kSmem, s, GATEUP && g.overlap, *g.w0, *g.w1,
+                                 *g.act_box, a);
 }
 
 }  // namespace

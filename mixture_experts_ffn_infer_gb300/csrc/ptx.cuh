@@ -89,6 +89,16 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t c0
                : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// The next kernel in the stream may be scheduled once every CTA of this grid has
+// executed this (or exited); it still waits in pdl_wait for this grid's results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grid this one was launched behind has completed and its writes
+// are visible (returns at once for a kernel launched without that attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
