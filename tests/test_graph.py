@@ -1,0 +1,68 @@
+"""The calls are asynchronous on the caller's stream with no host synchronisation,
+so a whole forward can be captured in a CUDA graph and replayed: the replay must
+give the eager result bit for bit, for both tile widths and the fused layer."""
+
+import pytest
+import torch
+
+import mixture_experts_ffn_infer_gb300 as mx
+from mixture_experts_ffn_infer_gb300 import synthetic as syn
+from tests import gpu_cases as cases
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["tiny", "k2_decode", syn.Workload("g16", 40, 512, 256, 32, 4, seed=21)])
+def test_infer_graph_replay_matches_eager(name):
+    c = cases.workload(name)
+    n, d = c.x.shape
+    k = c.ids.shape[1]
+    E, d_ff, _ = mx.bank_sizes(c.bank)
+    dm = mx.dims(d, d_ff, E, k)
+    bank = mx.pack_bank(c.bank)
+    W = mx.weights(bank)
+    ws = mx.workspace(dm, n)
+    x, ids, w = c.x.clone(), c.ids.clone(), c.w.clone()
+    out = torch.empty(n, d, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()   # packing and copies ran on the default stream; the calls below use their own
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        mx.moe_infer(dm, n, x, ids, w, W, out, ws, stream=s)   # first call outside the capture
+    s.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.moe_infer(dm, n, x, ids, w, W, out, ws, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    # new inputs in the same buffers: the graph reads them
+    x.copy_(torch.flip(c.x, dims=[0]))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, mx.infer(x, ids, w, c.bank))
+    assert mx.moe_get_error(ws) == mx.MOE_OK
+
+
+def test_layer_graph_replay_matches_eager():
+    wl = syn.Workload("blkg", 300, 384, 256, 3, 2, full_block=True, d_ff_shared=256, seed=11)
+    c = cases.workload(wl)
+    n, d = c.x.shape
+    dm = mx.dims(d, 256, 3, 2)
+    ws = mx.workspace(dm, n, 256)
+    out = torch.empty(n, d, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    W, WS = mx.weights(c.bank), mx.weights(c.shared)
+    with torch.cuda.stream(s):
+        mx.moe_layer_forward(dm, n, c.x, c.gain, c.inp.eps, c.ids, c.w, W, WS, 256, out, ws, stream=s)
+    s.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.moe_layer_forward(dm, n, c.x, c.gain, c.inp.eps, c.ids, c.w, W, WS, 256, out, ws, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
