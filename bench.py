@@ -326,7 +326,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        # the tensor cores multiply e4m3 weights by e4m3 activation terms and accumulate in fp32
+        "dtype": "e4m3",
         "data": "synthetic",
         "config": {"workload": args.workload, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
                    "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
