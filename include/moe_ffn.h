@@ -39,13 +39,16 @@
  *     n * k < 2^31.  Pointers handed to the tensor-memory-access engine
  *     (weights, x) must be 16-byte aligned; the workspace 256-byte aligned.
  *
- * Precision: the expert GEMMs multiply f16 operands (the e4m3 weight codes
- * and the bf16 activations both convert to f16 exactly, for |x| < 65504)
- * into fp32 accumulators; each 128 x 128 block scale multiplies its fp32
- * partial sum.  silu(g) * u is formed in fp32 and stored as f16 (h), each
- * weighted expert row is stored as f16, the k rows are summed in fp32 in
- * ascending slot order and the result is rounded once to bf16 (or kept in
- * fp32 when out_is_fp32 is set).
+ * Precision: the expert GEMMs multiply e4m3 operands on the tensor cores
+ * into fp32 accumulators.  Each activation row is carried as a sum of e4m3
+ * terms sharing one power-of-two scale per 128 columns: two terms hold a bf16
+ * value exactly (x, and the bf16 RMSNorm output) unless it lies more than
+ * 2^10 below its block's maximum (then within 2^-18 of that maximum), three
+ * terms carry silu(g) * u (h, formed in fp32) to about 12 significant bits.  Each
+ * 128 x 128 weight block scale and the activation scale multiply the fp32
+ * partial sum of their block.  Each weighted expert row is stored as f16, the
+ * k rows are summed in fp32 in ascending slot order and the result is rounded
+ * once to bf16 (or kept in fp32 when out_is_fp32 is set).
  */
 #ifndef MOE_FFN_H
 #define MOE_FFN_H
