@@ -49,18 +49,22 @@ def _configure(L):
     L.oracle_dequant.restype = dbl
     L.oracle_dequant.argtypes = [vp, vp, i64, i64, i64, i64]
     L.oracle_expert_forward.restype = None
-    L.oracle_expert_forward.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.oracle_expert_forward.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, i32]
+    L.oracle_e4m3_encode.restype = ctypes.c_uint8
+    L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    L.oracle_fp8_dynamic.restype = None
+    L.oracle_fp8_dynamic.argtypes = [i64, vp, vp, vp, vp]
     L.oracle_rmsnorm.restype = None
     L.oracle_rmsnorm.argtypes = [i64, i64, vp, vp, dbl, vp]
     L.oracle_permute.restype = i64
     L.oracle_permute.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
     L.oracle_moe_infer.restype = None
-    L.oracle_moe_infer.argtypes = [i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp, i64, vp, i32]
+    L.oracle_moe_infer.argtypes = [i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp, i64, vp, i32, i32]
     L.oracle_layer_forward.restype = None
     L.oracle_layer_forward.argtypes = ([i64, i64, i64, i64, vp, vp, dbl, vp, vp] + [vp] * 6
-                                       + [vp] * 6 + [i64, vp, i64, vp, i32])
+                                       + [vp] * 6 + [i64, vp, i64, vp, i32, i32])
     L.oracle_moe_infer_sorted.restype = None
-    L.oracle_moe_infer_sorted.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp]
+    L.oracle_moe_infer_sorted.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp] + [vp] * 6 + [vp, i32]
     return L
 
 
@@ -149,8 +153,28 @@ def dequant(q, s):
     return out
 
 
-def expert_forward(x, wg, sg, wu, su, wd, sd):
-    """One SwiGLU expert on fp64 rows x [n, d] -> [n, d]."""
+def e4m3_encode(v: float) -> int:
+    """Nearest e4m3 code of a float32 value (ties to even, saturating at 448)."""
+    return int(lib().oracle_e4m3_encode(float(v)))
+
+
+def fp8_dynamic(v):
+    """Dynamic FP8 quantisation of rows v [..., n] (n a multiple of 128), per group of 128 features.
+    Returns (dequantised fp64 values, e4m3 codes uint8, group scales float32 [..., n/128])."""
+    v = np.ascontiguousarray(np.asarray(v, np.float64))
+    n = v.shape[-1]
+    rows = v.reshape(-1, n)
+    out = np.empty_like(rows)
+    codes = np.empty(rows.shape, np.uint8)
+    scales = np.empty((rows.shape[0], n // 128), np.float32)
+    L = lib()
+    for i in range(rows.shape[0]):
+        L.oracle_fp8_dynamic(n, _ptr(rows[i]), _ptr(out[i]), _ptr(codes[i]), _ptr(scales[i]))
+    return (out.reshape(v.shape), codes.reshape(v.shape), scales.reshape(v.shape[:-1] + (n // 128,)))
+
+
+def expert_forward(x, wg, sg, wu, su, wd, sd, fp8_act=False):
+    """One SwiGLU expert on fp64 rows x [n, d] -> [n, d] (fp8_act: dynamic FP8 activations)."""
     x = np.ascontiguousarray(np.asarray(x, np.float64))
     n, d = x.shape
     wg, wu, wd = (_np(a, np.uint8) for a in (wg, wu, wd))
@@ -158,7 +182,7 @@ def expert_forward(x, wg, sg, wu, su, wd, sd):
     dff = wg.shape[0]
     out = np.empty((n, d), np.float64)
     lib().oracle_expert_forward(n, d, dff, _ptr(x), _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(wd),
-                                _ptr(sd), _ptr(out))
+                                _ptr(sd), _ptr(out), int(bool(fp8_act)))
     return out
 
 
@@ -184,8 +208,9 @@ def permute(topk_ids, num_experts: int):
     return counts, offsets, sp[:R], ip[:R], int(bad)
 
 
-def moe_infer(x, topk_ids, topk_weight, bank, tokens=None, threads=None):
-    """Routed sum for the selected tokens (default: all).  Returns fp64 [len(tokens), d]."""
+def moe_infer(x, topk_ids, topk_weight, bank, tokens=None, threads=None, fp8_act=False):
+    """Routed sum for the selected tokens (default: all).  Returns fp64 [len(tokens), d].
+    fp8_act: dynamic FP8 activations (per-128-feature e4m3 with scale amax/448)."""
     xb = _np(x, np.uint16)
     ids = _np(topk_ids, np.int32)
     w = _np(topk_weight, np.float32)
@@ -199,11 +224,12 @@ def moe_infer(x, topk_ids, topk_weight, bank, tokens=None, threads=None):
     b = _Bank(bank, used)
     y = np.empty((tok.size, d), np.float64)
     lib().oracle_moe_infer(d, dff, k, E, _ptr(xb), _ptr(ids), _ptr(w), *b.args(), _ptr(tok), tok.size, _ptr(y),
-                           threads or default_threads())
+                           threads or default_threads(), int(bool(fp8_act)))
     return y
 
 
-def layer_forward(hidden, gain, eps, topk_ids, topk_weight, bank, shared=None, tokens=None, threads=None):
+def layer_forward(hidden, gain, eps, topk_ids, topk_weight, bank, shared=None, tokens=None, threads=None,
+                  fp8_act=False):
     """Full block for the selected tokens: h + routed(RMSNorm(h)) + shared(RMSNorm(h)).  fp64."""
     hb = _np(hidden, np.uint16)
     gb = _np(gain, np.uint16)
@@ -228,11 +254,12 @@ def layer_forward(hidden, gain, eps, topk_ids, topk_weight, bank, shared=None, t
         dff_sh = 0
     y = np.empty((tok.size, d), np.float64)
     lib().oracle_layer_forward(d, dff, k, E, _ptr(hb), _ptr(gb), float(eps), _ptr(ids), _ptr(w), *b.args(),
-                               *sh_args, dff_sh, _ptr(tok), tok.size, _ptr(y), threads or default_threads())
+                               *sh_args, dff_sh, _ptr(tok), tok.size, _ptr(y), threads or default_threads(),
+                               int(bool(fp8_act)))
     return y
 
 
-def moe_infer_sorted(x, topk_ids, topk_weight, bank):
+def moe_infer_sorted(x, topk_ids, topk_weight, bank, fp8_act=False):
     """The sorted-slice form (small inputs only).  fp64 [n, d]."""
     xb = _np(x, np.uint16)
     ids = _np(topk_ids, np.int32)
@@ -243,7 +270,8 @@ def moe_infer_sorted(x, topk_ids, topk_weight, bank):
     dff = bank.w_gate.shape[1]
     b = _Bank(bank)
     y = np.empty((n, d), np.float64)
-    lib().oracle_moe_infer_sorted(n, d, dff, k, E, _ptr(xb), _ptr(ids), _ptr(w), *b.args(), _ptr(y))
+    lib().oracle_moe_infer_sorted(n, d, dff, k, E, _ptr(xb), _ptr(ids), _ptr(w), *b.args(), _ptr(y),
+                                  int(bool(fp8_act)))
     return y
 
 

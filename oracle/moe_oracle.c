@@ -41,7 +41,16 @@
  *   - everything after RMSNorm has no intermediate rounding (the exact
  *     function; the roundings an implementation does are covered by the
  *     parity tolerance);
- *   - summation order: ((sum over j ascending of w_j * E_j(x)) + shared(x)) + residual.
+ *   - summation order: ((sum over j ascending of w_j * E_j(x)) + shared(x)) + residual;
+ *   - dynamic FP8 activations (optional, the config's activation_scheme
+ *     "dynamic" with fmt e4m3): every row entering a linear (x or the
+ *     normalised row before gate/up, h before down) is quantised on the fly
+ *     per group of 128 consecutive features, the K extent of a weight block:
+ *     scale s = amax / 448 in float32 (1 when the group is all zero), code =
+ *     the e4m3 value nearest to v / s computed in float32 (ties to the even
+ *     code, magnitudes past 448 saturate), and the linear sees code * s.  h
+ *     is rounded to float32 before it is quantised, the precision the
+ *     decision is taken in.
  */
 #include <math.h>
 #include <pthread.h>
@@ -117,6 +126,61 @@ double oracle_silu(double a)
 }
 
 /* ------------------------------------------------------------------------- */
+/* Dynamic FP8 activations                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* The e4m3 code nearest to v: every finite non-negative code 0x00..0x7E is
+ * tried, a tie goes to the code with an even mantissa, and magnitudes past
+ * 448 land on 448 (the nearest finite value).  NaN gives 0x7F. */
+uint8_t oracle_e4m3_encode(float v)
+{
+    pthread_once(&g_once, init_tables);
+    if (v != v)
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    int best = 0;
+    double best_dist = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double dist = fabs(g_e4m3[c] - a);
+        if (dist < best_dist || (dist == best_dist && (c & 1) == 0)) {
+            best = c;
+            best_dist = dist;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* One row of n features (n a multiple of 128) under the dynamic scheme:
+ * out[i] = code_i * s_g for the group g = i / 128 holding i.  codes[n] and
+ * scales[n / 128] receive the codes and the group scales when not NULL. */
+void oracle_fp8_dynamic(int64_t n, const double *v, double *out, uint8_t *codes, float *scales)
+{
+    pthread_once(&g_once, init_tables);
+    for (int64_t g = 0; g < n / 128; ++g) {
+        const double *vg = v + g * 128;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < 128; ++i) {
+            float m = fabsf((float)vg[i]);
+            if (m > amax)
+                amax = m;
+        }
+        float s = amax / 448.0f;
+        if (!(s > 0.0f))
+            s = 1.0f;
+        for (int64_t i = 0; i < 128; ++i) {
+            float q = (float)vg[i] / s;
+            uint8_t code = oracle_e4m3_encode(q);
+            out[g * 128 + i] = g_e4m3[code] * (double)s;
+            if (codes)
+                codes[g * 128 + i] = code;
+        }
+        if (scales)
+            scales[g] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* One SwiGLU expert on one input row                                        */
 /* ------------------------------------------------------------------------- */
 
@@ -124,8 +188,11 @@ typedef struct {
     qmat gate, up, down;   /* gate/up: [d_ff, d], down: [d, d_ff] */
 } expert_t;
 
-/* out[d] = down( silu(gate x) * (up x) ); scratch holds 3 * d_ff doubles. */
-static void expert_row(const expert_t *ex, int64_t d, int64_t dff, const double *x, double *out, double *scratch)
+/* out[d] = down( silu(gate x) * (up x) ); scratch holds 3 * d_ff doubles.
+ * With fp8_act the row h is quantised under the dynamic scheme before down
+ * (x is the caller's, quantised already when the scheme is on). */
+static void expert_row(const expert_t *ex, int64_t d, int64_t dff, const double *x, double *out, double *scratch,
+                       int fp8_act)
 {
     double *g = scratch, *u = scratch + dff, *h = scratch + 2 * dff;
     for (int64_t f = 0; f < dff; ++f) {
@@ -139,6 +206,10 @@ static void expert_row(const expert_t *ex, int64_t d, int64_t dff, const double 
     }
     for (int64_t f = 0; f < dff; ++f)
         h[f] = oracle_silu(g[f]) * u[f];
+    if (fp8_act) {
+        oracle_fp8_dynamic(dff, h, g, NULL, NULL);
+        h = g;
+    }
     for (int64_t r = 0; r < d; ++r) {
         double acc = 0.0;
         for (int64_t f = 0; f < dff; ++f)
@@ -158,16 +229,25 @@ static expert_t make_expert(const uint8_t *const *wg, const float *const *sg, co
     return ex;
 }
 
-/* Single expert on a batch of rows, for pins against a library matmul. */
+/* Single expert on a batch of rows, for pins against a library matmul.  With
+ * fp8_act each row is quantised under the dynamic scheme first. */
 void oracle_expert_forward(int64_t n_rows, int64_t d, int64_t dff, const double *x, const uint8_t *wg,
                            const float *sg, const uint8_t *wu, const float *su, const uint8_t *wd,
-                           const float *sd, double *out)
+                           const float *sd, double *out, int fp8_act)
 {
     pthread_once(&g_once, init_tables);
     expert_t ex = {{wg, sg, dff, d}, {wu, su, dff, d}, {wd, sd, d, dff}};
     double *scratch = (double *)malloc(sizeof(double) * 3 * dff);
-    for (int64_t i = 0; i < n_rows; ++i)
-        expert_row(&ex, d, dff, x + i * d, out + i * d, scratch);
+    double *xq = (double *)malloc(sizeof(double) * d);
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const double *xi = x + i * d;
+        if (fp8_act) {
+            oracle_fp8_dynamic(d, xi, xq, NULL, NULL);
+            xi = xq;
+        }
+        expert_row(&ex, d, dff, xi, out + i * d, scratch, fp8_act);
+    }
+    free(xq);
     free(scratch);
 }
 
@@ -270,6 +350,7 @@ typedef struct {
     const uint8_t *shg, *shu, *shd;  /* shared expert, or NULL */
     const float *ssg, *ssu, *ssd;
     int64_t dff_sh;
+    int fp8_act;                  /* dynamic FP8 activations */
     /* work */
     const int64_t *tok;           /* token indices to evaluate */
     int64_t n_tok;
@@ -305,6 +386,8 @@ static void *token_worker(void *arg)
         else
             for (int64_t c = 0; c < d; ++c)
                 xin[c] = oracle_bf16_value(jb->x[t * d + c]);
+        if (jb->fp8_act)
+            oracle_fp8_dynamic(d, xin, xin, NULL, NULL);
         for (int64_t c = 0; c < d; ++c)
             acc[c] = 0.0;
         for (int64_t j = 0; j < k; ++j) {
@@ -312,7 +395,7 @@ static void *token_worker(void *arg)
             if (e < 0 || e >= jb->E)
                 continue;
             expert_t ex = make_expert(jb->wg, jb->sg, jb->wu, jb->su, jb->wd, jb->sd, e, d, dff);
-            expert_row(&ex, d, dff, xin, o, scratch);
+            expert_row(&ex, d, dff, xin, o, scratch, jb->fp8_act);
             double wt = (double)jb->w[t * k + j];
             for (int64_t c = 0; c < d; ++c)
                 acc[c] += wt * o[c];
@@ -320,7 +403,7 @@ static void *token_worker(void *arg)
         if (jb->shg) {
             expert_t sh = {{jb->shg, jb->ssg, jb->dff_sh, d}, {jb->shu, jb->ssu, jb->dff_sh, d},
                            {jb->shd, jb->ssd, d, jb->dff_sh}};
-            expert_row(&sh, d, jb->dff_sh, xin, o, scratch);
+            expert_row(&sh, d, jb->dff_sh, xin, o, scratch, jb->fp8_act);
             for (int64_t c = 0; c < d; ++c)
                 acc[c] += o[c];
         }
@@ -356,11 +439,11 @@ static void run_job(job_t *jb, int nthreads)
 void oracle_moe_infer(int64_t d, int64_t dff, int64_t k, int64_t E, const uint16_t *x, const int32_t *ids,
                       const float *w, const uint8_t *const *wg, const float *const *sg, const uint8_t *const *wu,
                       const float *const *su, const uint8_t *const *wd, const float *const *sd,
-                      const int64_t *tok, int64_t n_tok, double *y, int nthreads)
+                      const int64_t *tok, int64_t n_tok, double *y, int nthreads, int fp8_act)
 {
     job_t jb;
     memset(&jb, 0, sizeof jb);
-    jb.d = d; jb.dff = dff; jb.k = k; jb.E = E;
+    jb.d = d; jb.dff = dff; jb.k = k; jb.E = E; jb.fp8_act = fp8_act;
     jb.x = x; jb.ids = ids; jb.w = w;
     jb.wg = wg; jb.sg = sg; jb.wu = wu; jb.su = su; jb.wd = wd; jb.sd = sd;
     jb.tok = tok; jb.n_tok = n_tok; jb.y = y;
@@ -376,11 +459,11 @@ void oracle_layer_forward(int64_t d, int64_t dff, int64_t k, int64_t E, const ui
                           const float *const *su, const uint8_t *const *wd, const float *const *sd,
                           const uint8_t *shg, const float *ssg, const uint8_t *shu, const float *ssu,
                           const uint8_t *shd, const float *ssd, int64_t dff_sh, const int64_t *tok,
-                          int64_t n_tok, double *y, int nthreads)
+                          int64_t n_tok, double *y, int nthreads, int fp8_act)
 {
     job_t jb;
     memset(&jb, 0, sizeof jb);
-    jb.d = d; jb.dff = dff; jb.k = k; jb.E = E;
+    jb.d = d; jb.dff = dff; jb.k = k; jb.E = E; jb.fp8_act = fp8_act;
     jb.x = hidden; jb.ids = ids; jb.w = w;
     jb.wg = wg; jb.sg = sg; jb.wu = wu; jb.su = su; jb.wd = wd; jb.sd = sd;
     jb.resid = hidden; jb.gain = gain; jb.eps = eps;
@@ -403,7 +486,7 @@ void oracle_layer_forward(int64_t d, int64_t dff, int64_t k, int64_t E, const ui
 void oracle_moe_infer_sorted(int64_t n, int64_t d, int64_t dff, int64_t k, int64_t E, const uint16_t *x,
                              const int32_t *ids, const float *w, const uint8_t *const *wg,
                              const float *const *sg, const uint8_t *const *wu, const float *const *su,
-                             const uint8_t *const *wd, const float *const *sd, double *y)
+                             const uint8_t *const *wd, const float *const *sd, double *y, int fp8_act)
 {
     pthread_once(&g_once, init_tables);
     int64_t R = n * k;
@@ -421,6 +504,8 @@ void oracle_moe_infer_sorted(int64_t n, int64_t d, int64_t dff, int64_t k, int64
         int64_t t = idxs[i] / k;
         for (int64_t c = 0; c < d; ++c)
             sorted_tokens[i * d + c] = oracle_bf16_value(x[t * d + c]);
+        if (fp8_act)
+            oracle_fp8_dynamic(d, sorted_tokens + i * d, sorted_tokens + i * d, NULL, NULL);
     }
     int64_t start = 0;
     for (int64_t e = 0; e < E; ++e) {
@@ -429,7 +514,7 @@ void oracle_moe_infer_sorted(int64_t n, int64_t d, int64_t dff, int64_t k, int64
             continue;
         expert_t ex = make_expert(wg, sg, wu, su, wd, sd, e, d, dff);
         for (int64_t i = start; i < end; ++i)
-            expert_row(&ex, d, dff, sorted_tokens + i * d, outs + i * d, scratch);
+            expert_row(&ex, d, dff, sorted_tokens + i * d, outs + i * d, scratch, fp8_act);
         start = end;
     }
     for (int64_t i = 0; i < nvalid; ++i)

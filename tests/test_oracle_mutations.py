@@ -2,7 +2,8 @@
 
 Each case plants one plausible slip in a temporary copy of the oracle's C
 source (a dropped term, a swapped operand, a wrong index, an unstable sort, a
-lost weight, an off-by-one exponent, a missing residual or shared expert),
+lost weight, an off-by-one exponent, a missing residual or shared expert, a
+wrong FP8 activation scale, group, rounding or a skipped quantisation),
 builds it with gcc, swaps it in and checks that at least one pin of
 test_oracle_pins.py fails.  The committed oracle is never modified."""
 
@@ -34,6 +35,14 @@ MUTATIONS = {
     "residual dropped": ("acc[c] += oracle_bf16_value(jb->resid[t * d + c]);", "(void)0;"),
     "shared expert dropped": ("            for (int64_t c = 0; c < d; ++c)\n                acc[c] += o[c];\n        }",
                               "        }"),
+    "fp8 scale for a 240 maximum": ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
+    "fp8 amax over the rest of the row": ("        for (int64_t i = 0; i < 128; ++i) {\n            float m",
+                                          "        for (int64_t i = 0; i < n - g * 128; ++i) {\n            float m"),
+    "fp8 ties to the odd code": ("(dist == best_dist && (c & 1) == 0)", "(dist == best_dist && (c & 1) == 1)"),
+    "fp8 h not quantised": ("    if (fp8_act) {\n        oracle_fp8_dynamic(dff, h, g, NULL, NULL);\n        h = g;\n    }",
+                            ""),
+    "fp8 token row not quantised": ("        if (jb->fp8_act)\n            oracle_fp8_dynamic(d, xin, xin, NULL, NULL);",
+                                    ""),
 }
 
 # the pins, with one parameter set each where they are parametrised
@@ -53,6 +62,12 @@ PINS = [
     (pins.test_routed_sum_is_linear_in_router_weights_and_uses_each_slot, {}),
     (pins.test_layer_forward_matches_fp64_restatement, {}),
     (pins.test_layer_forward_zero_router_weights_no_shared_is_identity, {}),
+    (pins.test_e4m3_encode_matches_torch_cast_and_saturates, {}),
+    (pins.test_fp8_dynamic_group_invariants, {}),
+    (pins.test_fp8_dynamic_groups_are_independent_and_scale_equivariant, {}),
+    (pins.test_expert_fp8_act_matches_torch_restatement, {}),
+    (pins.test_moe_infer_fp8_act_matches_torch_restatement_tiny, {}),
+    (pins.test_layer_forward_fp8_act_quantises_the_normalised_row_and_shared_expert, {}),
 ]
 
 

@@ -376,3 +376,160 @@ def test_layer_forward_zero_router_weights_no_shared_is_identity():
     inp = syn.make_inputs(wl)
     y = oracle.layer_forward(inp.x, inp.gain, inp.eps, inp.topk_ids, torch.zeros_like(inp.topk_weight), inp.bank)
     assert np.array_equal(y, inp.x.double().numpy())
+
+
+# ---------------------------------------------------------------- dynamic FP8 activations
+#
+# "Input features" page, quantisation config: fmt e4m3, activation_scheme
+# "dynamic", weight blocks of 128 x 128.  The oracle quantises every row
+# entering a linear per group of 128 features (scale amax / 448 in float32,
+# code = nearest e4m3 of v / s, ties to even, saturating).
+
+
+def _torch_e4m3_codes(v32):
+    """torch's float32 -> float8_e4m3fn cast (round to nearest, ties to even) as code bytes."""
+    return v32.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def test_e4m3_encode_matches_torch_cast_and_saturates():
+    g = torch.Generator().manual_seed(21)
+    vals = torch.tensor([oracle.e4m3_value(c) for c in range(0x7F)], dtype=torch.float64)
+    mids = (vals[1:] + vals[:-1]) / 2              # exact ties between neighbouring codes
+    pts = torch.cat([vals, mids, mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20),
+                     torch.rand(4000, generator=g, dtype=torch.float64) * 448,
+                     torch.rand(2000, generator=g, dtype=torch.float64) * 2.0 ** -6])
+    pts = torch.cat([pts, -pts]).float()
+    ref = _torch_e4m3_codes(pts)
+    ours = torch.tensor([oracle.e4m3_encode(float(v)) for v in pts], dtype=torch.uint8)
+    assert torch.equal(ours, ref)
+    # past the largest finite value the encoder saturates (torch's cast gives NaN there)
+    for v, c in ((448.0, 0x7E), (460.0, 0x7E), (1e6, 0x7E), (-1e6, 0xFE)):
+        assert oracle.e4m3_encode(v) == c
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def _fp8_rows():
+    g = torch.Generator().manual_seed(22)
+    v = torch.randn(3, 512, generator=g, dtype=torch.float64)
+    v[:, 128:256] *= 1e-3        # groups of very different size in one row
+    v[:, 256:384] *= 300.0
+    v[1, 384:] = 0.0             # an all-zero group
+    return v.float().double()    # float32 inputs
+
+
+def test_fp8_dynamic_group_invariants():
+    v = _fp8_rows()
+    deq, codes, scales = oracle.fp8_dynamic(v.numpy())
+    vn = v.numpy()
+    assert scales.shape == (3, 4)
+    for r in range(3):
+        for gi in range(4):
+            sl = slice(128 * gi, 128 * (gi + 1))
+            grp, c, s = vn[r, sl], codes[r, sl], float(scales[r, gi])
+            if not np.any(grp):
+                assert s == 1.0 and not np.any(deq[r, sl]) and np.all((c & 0x7F) == 0)
+                continue
+            # the group's largest magnitude takes the largest code and nothing saturates:
+            # 448 * s covers amax up to float32 rounding
+            assert (c & 0x7F).max() == 0x7E
+            amax = np.abs(grp).max()
+            assert 448.0 * s >= amax * (1 - 2.0 ** -22) and 448.0 * s <= amax * (1 + 2.0 ** -22)
+            # round to nearest: within half an e4m3 step (2^-4 relative, 2^-10 * s in the subnormals)
+            err = np.abs(deq[r, sl] - grp)
+            assert np.all(err <= 2.0 ** -4 * np.abs(grp) + 2.0 ** -10 * s)
+            # codes times the scale are the returned values
+            vals = np.array([oracle.e4m3_value(int(x)) for x in c])
+            assert np.array_equal(deq[r, sl], vals * s)
+            # the codes are torch's cast of v / s (float32 division)
+            q = torch.from_numpy(grp.astype(np.float32)) / torch.tensor(s, dtype=torch.float32)
+            assert torch.equal(_torch_e4m3_codes(q), torch.from_numpy(c.copy()))
+
+
+def test_fp8_dynamic_groups_are_independent_and_scale_equivariant():
+    v = _fp8_rows()
+    deq, codes, scales = oracle.fp8_dynamic(v.numpy())
+    w = v.clone()
+    w[:, 256:384] *= 1e4                           # only group 2 changes
+    deq2, codes2, scales2 = oracle.fp8_dynamic(w.numpy())
+    keep = np.r_[0:256, 384:512]
+    assert np.array_equal(deq[:, keep], deq2[:, keep]) and np.array_equal(scales[:, [0, 1, 3]],
+                                                                          scales2[:, [0, 1, 3]])
+    # a power-of-two factor moves only the scales
+    deq3, codes3, scales3 = oracle.fp8_dynamic((v * 32.0).numpy())
+    nz = scales != 1.0
+    assert np.array_equal(codes3, codes) and np.array_equal(scales3[nz], scales[nz] * 32.0)
+    assert np.array_equal(deq3, deq * 32.0)
+
+
+def _torch_fp8_dynamic(v):
+    """Per-128-feature dynamic quantisation restated with torch: float32 amax / 448, torch's e4m3 cast."""
+    v32 = v.float()
+    grp = v32.reshape(*v32.shape[:-1], -1, 128)
+    s = grp.abs().amax(-1, keepdim=True) / 448.0
+    s = torch.where(s > 0, s, torch.ones_like(s))
+    q = (grp / s).clamp(-448, 448).to(torch.float8_e4m3fn).to(torch.float64)
+    return (q * s.double()).reshape(v.shape)
+
+
+def test_expert_fp8_act_matches_torch_restatement():
+    d, dff = 256, 384
+    b = _small_bank(1, d, dff, seed=11)
+    x = torch.randn(5, d, dtype=torch.float64, generator=torch.Generator().manual_seed(5))
+    Wg = _deq_torch(b.w_gate[0], b.s_gate[0])
+    Wu = _deq_torch(b.w_up[0], b.s_up[0])
+    Wd = _deq_torch(b.w_down[0], b.s_down[0])
+    xq = _torch_fp8_dynamic(x)
+    h = F.silu(xq @ Wg.T) * (xq @ Wu.T)
+    ref = _torch_fp8_dynamic(h) @ Wd.T
+    ours = oracle.expert_forward(x.numpy(), b.w_gate[0], b.s_gate[0], b.w_up[0], b.s_up[0],
+                                 b.w_down[0], b.s_down[0], fp8_act=True)
+    assert np.allclose(ours, ref.numpy(), rtol=1e-12, atol=1e-14)
+    # the scheme changes the result by about an e4m3 step, not by nothing
+    exact = oracle.expert_forward(x.numpy(), b.w_gate[0], b.s_gate[0], b.w_up[0], b.s_up[0],
+                                  b.w_down[0], b.s_down[0])
+    rel = np.abs(ours - exact).mean() / np.abs(exact).mean()
+    assert 3e-3 < rel < 1e-1
+
+
+def test_moe_infer_fp8_act_matches_torch_restatement_tiny():
+    inp = syn.make_inputs(syn.WORKLOADS["tiny"], n_tokens=24)
+    ours = oracle.moe_infer(inp.x, inp.topk_ids, inp.topk_weight, inp.bank, fp8_act=True)
+    xq = _torch_fp8_dynamic(inp.x.double())
+    n, k = inp.topk_ids.shape
+    ref = torch.zeros(n, inp.x.shape[1], dtype=torch.float64)
+    for t in range(n):
+        for j in range(k):
+            e = int(inp.topk_ids[t, j])
+            Wg = _deq_torch(inp.bank.w_gate[e], inp.bank.s_gate[e])
+            Wu = _deq_torch(inp.bank.w_up[e], inp.bank.s_up[e])
+            Wd = _deq_torch(inp.bank.w_down[e], inp.bank.s_down[e])
+            h = F.silu(Wg @ xq[t]) * (Wu @ xq[t])
+            ref[t] += float(inp.topk_weight[t, j]) * (Wd @ _torch_fp8_dynamic(h[None])[0])
+    rel = np.abs(ours - ref.numpy()).max() / np.abs(ref.numpy()).max()
+    assert rel < 1e-12
+    # the sorted-slice form does the same arithmetic
+    sorted_form = oracle.moe_infer_sorted(inp.x, inp.topk_ids, inp.topk_weight, inp.bank, fp8_act=True)
+    assert np.array_equal(sorted_form, ours)
+
+
+def test_layer_forward_fp8_act_quantises_the_normalised_row_and_shared_expert():
+    wl = syn.Workload("blk", 6, 256, 128, 8, 3, full_block=True, d_ff_shared=256, seed=6)
+    inp = syn.make_inputs(wl)
+    y = oracle.layer_forward(inp.x, inp.gain, inp.eps, inp.topk_ids, inp.topk_weight, inp.bank, inp.shared,
+                             fp8_act=True)
+    xn = torch.from_numpy(oracle.rmsnorm(inp.x, inp.gain, inp.eps))
+    xq = _torch_fp8_dynamic(xn)
+
+    def expert(bank, e, row):
+        Wg = _deq_torch(bank.w_gate[e], bank.s_gate[e])
+        Wu = _deq_torch(bank.w_up[e], bank.s_up[e])
+        Wd = _deq_torch(bank.w_down[e], bank.s_down[e])
+        return Wd @ _torch_fp8_dynamic((F.silu(Wg @ row) * (Wu @ row))[None])[0]
+
+    n, k = inp.topk_ids.shape
+    ref = torch.zeros(n, wl.d, dtype=torch.float64)
+    for t in range(n):
+        for j in range(k):
+            ref[t] += float(inp.topk_weight[t, j]) * expert(inp.bank, int(inp.topk_ids[t, j]), xq[t])
+        ref[t] = inp.x[t].double() + (ref[t] + expert(inp.shared, 0, xq[t]))
+    assert np.allclose(y, ref.numpy(), rtol=1e-11, atol=1e-12)
