@@ -198,7 +198,8 @@ def run_ours(args, rank, world, local_rank):
     n = x.shape[0]
     xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
     gaind = gain.to(dev) if gain is not None else None
-    dm = mx.dims(wl.d, wl.d_ff, wl.num_experts, wl.top_k)
+    fp8 = args.act == "fp8"
+    dm = mx.dims(wl.d, wl.d_ff, wl.num_experts, wl.top_k, mx.MOE_ACT_FP8_DYNAMIC if fp8 else mx.MOE_ACT_EXACT)
     dff_sh = wl.d_ff_shared if wl.full_block else 0
     ws = mx.workspace(dm, n, dff_sh, dev)
     out = torch.empty(n, wl.d, dtype=torch.bfloat16, device=dev)
@@ -314,7 +315,8 @@ def run_ours(args, rank, world, local_rank):
     step_roof_ms = alg["step_bytes"] / (hbm * 1e9) * 1e3
     bf16, bf16_src = _bf16_peak(sustained=True)
     tflops = alg["step_flops"] / (ms_step / 1e3) / 1e12
-    traffic = _traffic(args.workload, dominant)
+    # the recorded counters are of the exact scheme's kernels
+    traffic = _traffic(args.workload, dominant) if not fp8 else None
     result = {
         "metric": METRIC,
         "value": value,
@@ -332,6 +334,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
                    "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
                    "full_block": wl.full_block, "weights": "e4m3, fp32 scale per 128x128 block, tiled layout",
+                   "act_scheme": "fp8_dynamic" if fp8 else "exact",
                    "touched_experts": alg["touched_experts"],
                    "l2": "inputs larger than L2: %.2f GB of touched expert weights per step" % (
                        alg["step_bytes"] / 1e9),
@@ -346,7 +349,7 @@ def run_ours(args, rank, world, local_rank):
                           if kern_ms.get("down_scatter") else None,
                           "frac": (alg["down_bytes"] / (kern_ms["down_scatter"] / 1e3) / 1e9 / hbm)
                           if kern_ms.get("down_scatter") else None,
-                          "traffic": _traffic(args.workload, "down_scatter")},
+                          "traffic": _traffic(args.workload, "down_scatter") if not fp8 else None},
         "step_roofline": {"bytes": alg["step_bytes"], "flops": alg["step_flops"], "t_roof_ms_hbm": step_roof_ms,
                           "frac_hbm": step_roof_ms / ms_step, "tflops": tflops,
                           "frac_bf16_sustained": tflops / bf16, "bf16_peak_source": bf16_src},
@@ -358,11 +361,12 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=args.cpu_budget,
+                                              fp8=fp8)
     return result
 
 
-def _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s):
+def _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s, fp8=False):
     """Time the oracle on a token sample; returns (tokens/s, tokens, seconds, threads)."""
     import oracle
     import torch
@@ -372,9 +376,10 @@ def _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s):
     threads = oracle.default_threads()
     t0 = time.perf_counter()
     if wl.full_block:
-        oracle.layer_forward(x, gain, 1e-6, ids, w, bank_h, _HostBank(shared, [0]), tokens=tokens, threads=threads)
+        oracle.layer_forward(x, gain, 1e-6, ids, w, bank_h, _HostBank(shared, [0]), tokens=tokens, threads=threads,
+                             fp8_act=fp8)
     else:
-        oracle.moe_infer(x, ids, w, bank_h, tokens=tokens, threads=threads)
+        oracle.moe_infer(x, ids, w, bank_h, tokens=tokens, threads=threads, fp8_act=fp8)
     dt = time.perf_counter() - t0
     return n_tok / dt, n_tok, dt, threads
 
@@ -397,11 +402,11 @@ class _Sparse:
         return self.rows[int(e)]
 
 
-def cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=20.0):
+def cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=20.0, fp8=False):
     # sample: the first tokens of the batch; one probe token sizes the sample to the budget
-    rate1, _, dt1, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, 1, budget_s)
+    rate1, _, dt1, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, 1, budget_s, fp8)
     n_tok = max(1, min(4096, int(budget_s / max(dt1, 1e-3) * max(1, threads))))
-    rate, n_tok, dt, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s)
+    rate, n_tok, dt, threads = _oracle_rate(wl, x, ids, w, gain, bank, shared, n_tok, budget_s, fp8)
     return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{n_tok} token evaluations cycling over the {x.shape[0]}-token {wl.name} batch "
                       f"(fp64 C oracle, one thread per token), {dt:.1f} s"}
@@ -428,10 +433,12 @@ def run_reference(args):
         used = torch.unique(ids[tok]).tolist()
         hb = _HostBank(bank, used)
         t0 = time.perf_counter()
+        fp8 = args.act == "fp8"
         if wl.full_block:
-            oracle.layer_forward(x, gain, 1e-6, ids, w, hb, _HostBank(shared, [0]), tokens=tok, threads=threads)
+            oracle.layer_forward(x, gain, 1e-6, ids, w, hb, _HostBank(shared, [0]), tokens=tok, threads=threads,
+                                 fp8_act=fp8)
         else:
-            oracle.moe_infer(x, ids, w, hb, tokens=tok, threads=threads)
+            oracle.moe_infer(x, ids, w, hb, tokens=tok, threads=threads, fp8_act=fp8)
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
@@ -452,7 +459,8 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.workload, "n_tokens_per_gpu": x.shape[0], "d": wl.d, "d_ff": wl.d_ff,
-                   "num_experts": wl.num_experts, "top_k": wl.top_k},
+                   "num_experts": wl.num_experts, "top_k": wl.top_k,
+                   "act_scheme": "fp8_dynamic" if args.act == "fp8" else "exact"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{per_step} tokens of the {wl.name} batch per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -475,6 +483,8 @@ def main():
     ap.add_argument("--n-tokens", type=int, default=0,
                     help="override N (with --num-experts: a small case of the same rows per expert)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--act", default="exact", choices=["exact", "fp8"],
+                    help="activation scheme: exact split terms (default) or dynamic FP8 (per-128 e4m3, amax/448)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

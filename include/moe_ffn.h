@@ -36,11 +36,13 @@
  *   - n = 0 is a no-op that returns MOE_OK.  Experts that no token selects
  *     cost nothing (they are skipped, as the page's loop skips them).
  *   - Limits: d and d_ff multiples of 128, 1 <= E <= 1024, 1 <= k <= 32,
+ *     act_scheme one of the MOE_ACT_* values,
  *     n * k < 2^31.  Pointers handed to the tensor-memory-access engine
  *     (weights, x) must be 16-byte aligned; the workspace 256-byte aligned.
  *
  * Precision: the expert GEMMs multiply e4m3 operands on the tensor cores
- * into fp32 accumulators.  Each activation row is carried as a sum of e4m3
+ * into fp32 accumulators.  Under MOE_ACT_EXACT (the default; moe_dims
+ * below also offers dynamic FP8 activations) each activation row is carried as a sum of e4m3
  * terms sharing one power-of-two scale per 128 columns: two terms hold a bf16
  * value exactly (x, and the bf16 RMSNorm output) unless it lies more than
  * 2^10 below its block's maximum (then within 2^-18 of that maximum), three
@@ -72,13 +74,31 @@ typedef enum {
     MOE_ERR_CUDA = 7           /* a CUDA runtime call or launch failed */
 } moe_status;
 
+/* Activation schemes ("Input features" page, quantisation config: fmt e4m3,
+ * activation_scheme "dynamic", weight blocks of 128 x 128).
+ *   MOE_ACT_EXACT        every activation row is carried exactly as e4m3
+ *                        split terms (see Precision above); the result is
+ *                        the unquantised function of the FP8 weights.
+ *   MOE_ACT_FP8_DYNAMIC  every row entering a linear (x, the normalised row,
+ *                        h) is quantised on the fly per group of 128
+ *                        features: scale s = amax / 448 in fp32 (1 for an
+ *                        all-zero group), code = e4m3 nearest to v / s (ties
+ *                        to even, saturating at 448), the linear sees
+ *                        code * s.  One e4m3 term per value: half the tensor
+ *                        work of the exact scheme for gate/up, a third for
+ *                        down, at the accuracy of e4m3 activations. */
+#define MOE_ACT_EXACT 0
+#define MOE_ACT_FP8_DYNAMIC 1
+
 /* Problem dimensions: d = model width, d_ff = routed expert width,
- * num_experts = E, top_k = k. */
+ * num_experts = E, top_k = k, act_scheme = MOE_ACT_EXACT (0, what a
+ * zero-initialised struct gives) or MOE_ACT_FP8_DYNAMIC. */
 typedef struct {
     int32_t d;
     int32_t d_ff;
     int32_t num_experts;
     int32_t top_k;
+    int32_t act_scheme;
 } moe_dims;
 
 /* Layout of the e4m3 codes of a bank. */

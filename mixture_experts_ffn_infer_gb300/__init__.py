@@ -36,7 +36,11 @@ class MoeError(RuntimeError):
 
 class moe_dims(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("num_experts", ctypes.c_int32),
-                ("top_k", ctypes.c_int32)]
+                ("top_k", ctypes.c_int32), ("act_scheme", ctypes.c_int32)]
+
+
+MOE_ACT_EXACT = 0          # activations carried exactly as e4m3 split terms
+MOE_ACT_FP8_DYNAMIC = 1    # per-128-feature e4m3 activations, scale amax / 448
 
 
 MOE_LAYOUT_ROW_MAJOR = 0
@@ -128,8 +132,8 @@ def _check(status: int, where: str):
         raise MoeError(status, where)
 
 
-def dims(d: int, d_ff: int, num_experts: int, top_k: int) -> moe_dims:
-    return moe_dims(d, d_ff, num_experts, top_k)
+def dims(d: int, d_ff: int, num_experts: int, top_k: int, act_scheme: int = MOE_ACT_EXACT) -> moe_dims:
+    return moe_dims(d, d_ff, num_experts, top_k, act_scheme)
 
 
 def weights(bank) -> moe_weights:
@@ -283,11 +287,11 @@ def permute(topk_ids, num_experts: int, ws=None, validate=False, stream=None):
     return counts, offsets, sp[: n * k], ip[: n * k]
 
 
-def infer(x, topk_ids, topk_weight, bank, ws=None, out_is_fp32=False, stream=None):
+def infer(x, topk_ids, topk_weight, bank, ws=None, out_is_fp32=False, stream=None, act_scheme=MOE_ACT_EXACT):
     import torch
     n, d = x.shape
     E, d_ff, _ = bank_sizes(bank)
-    dm = moe_dims(d, d_ff, E, topk_ids.shape[1])
+    dm = moe_dims(d, d_ff, E, topk_ids.shape[1], act_scheme)
     if ws is None:
         ws = workspace(dm, n, 0, x.device)
     out = torch.empty(n, d, dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=x.device)
@@ -296,11 +300,11 @@ def infer(x, topk_ids, topk_weight, bank, ws=None, out_is_fp32=False, stream=Non
 
 
 def layer_forward(hidden, gain, eps, topk_ids, topk_weight, bank, shared=None, ws=None, out_is_fp32=False,
-                  stream=None):
+                  stream=None, act_scheme=MOE_ACT_EXACT):
     import torch
     n, d = hidden.shape
     E, d_ff, _ = bank_sizes(bank)
-    dm = moe_dims(d, d_ff, E, topk_ids.shape[1])
+    dm = moe_dims(d, d_ff, E, topk_ids.shape[1], act_scheme)
     dff_sh = bank_sizes(shared)[1] if shared is not None else 0
     if ws is None:
         ws = workspace(dm, n, dff_sh, hidden.device)

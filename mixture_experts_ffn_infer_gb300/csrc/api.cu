@@ -33,8 +33,15 @@ size_t align_up(size_t v) { return (v + 1023) & ~size_t(1023); }
 
 bool dims_ok(const moe_dims* d) {
   return d && d->d > 0 && d->d_ff > 0 && d->d % 128 == 0 && d->d_ff % 128 == 0 && d->num_experts >= 1 &&
-         d->num_experts <= kMaxExperts && d->top_k >= 1 && d->top_k <= kMaxTopK;
+         d->num_experts <= kMaxExperts && d->top_k >= 1 && d->top_k <= kMaxTopK &&
+         (d->act_scheme == MOE_ACT_EXACT || d->act_scheme == MOE_ACT_FP8_DYNAMIC);
 }
+
+bool fp8_act(const moe_dims* d) { return d->act_scheme == MOE_ACT_FP8_DYNAMIC; }
+
+// Activation terms the GEMMs read: bf16 rows (x, the normalised row) and h.
+int x_terms_of(bool fp8) { return fp8 ? 1 : 2; }
+int h_terms_of(bool fp8) { return fp8 ? 1 : 3; }
 
 bool make_layout(const moe_dims* d, int64_t n, int32_t dff_sh, Layout* L) {
   if (!dims_ok(d) || n < 0 || dff_sh < 0 || dff_sh % 128 != 0) return false;
@@ -140,8 +147,8 @@ bool map_act_planar(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows,
 
 // The split layout of `rows` sorted rows of width K, as the tile width chosen for
 // `rows` rows over `experts` experts reads it.
-SplitLayout rows_layout(int64_t rows, int64_t experts, int64_t K, int terms) {
-  return split_layout(tile_tokens(rows, experts) == kNTokWide, rows, K, terms);
+SplitLayout rows_layout(int64_t rows, int64_t experts, int64_t K, int terms, bool fp8) {
+  return split_layout(tile_tokens(rows, experts) == kNTokWide, rows, K, terms, fp8);
 }
 
 int num_sms() {
@@ -232,8 +239,9 @@ struct ActMaps {
 // Gate/up then down over `rows` sorted rows whose codes are already in xs (in
 // the layout rows_layout gives, x_terms terms), tiles cut at tile_tokens(rows,
 // experts) rows.  Down writes f16(topk_weight * o) to out[sorted_pos[row]]
-// (identity and weight 1 when those are null).
-moe_status run_gemms(bool after_gather, const moe_weights* w, int64_t d, int64_t dff, int64_t experts,
+// (identity and weight 1 when those are null).  fp8: dynamic FP8 activations
+// (x and h one term each).
+moe_status run_gemms(bool after_gather, bool fp8, const moe_weights* w, int64_t d, int64_t dff, int64_t experts,
                      int32_t rows, int x_terms,
                      uint8_t* xs, float* xs_inv, uint8_t* h, float* h_inv, TileDesc* tiles, int32_t* n_tiles,
                      const int32_t* sorted_pos, const float* topk_weight, void* out, uint32_t* err, cudaStream_t s,
@@ -241,7 +249,8 @@ moe_status run_gemms(bool after_gather, const moe_weights* w, int64_t d, int64_t
   const int ntok = tile_tokens(rows, experts);
   const bool wide = ntok == kNTokWide;
   ActMaps mx, mh;
-  if (!mx.make(wide, xs, d, rows, x_terms) || !mh.make(wide, h, dff, rows, 3)) return MOE_ERR_CUDA;
+  const int h_terms = h_terms_of(fp8);
+  if (!mx.make(wide, xs, d, rows, x_terms) || !mh.make(wide, h, dff, rows, h_terms)) return MOE_ERR_CUDA;
   CUtensorMap m_g, m_u, m_d;
   m_g = m_u = m_d = mx.m16;  // placeholders when the bank is tiled
   if (!map_bank(w, d, dff, experts, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;
@@ -249,6 +258,7 @@ moe_status run_gemms(bool after_gather, const moe_weights* w, int64_t d, int64_t
   GemmLaunch g{};
   g.ntok = ntok;
   g.terms = x_terms;
+  g.fp8 = fp8;
   g.w0 = &m_g;
   g.w1 = &m_u;
   g.w_tiled = tiled ? w->w_gate : nullptr;
@@ -273,7 +283,7 @@ moe_status run_gemms(bool after_gather, const moe_weights* w, int64_t d, int64_t
 
   GemmLaunch q = g;
   q.overlap = false;
-  q.terms = 3;
+  q.terms = h_terms;
   q.w0 = &m_d;
   q.w1 = &m_d;
   q.w_tiled = tiled ? w->w_down : nullptr;
@@ -295,7 +305,8 @@ moe_status run_gemms(bool after_gather, const moe_weights* w, int64_t d, int64_t
 // The expert pass on an already-sorted routing plan: gather, gate/up, down.
 // `gather` selects the bf16 row gather (moe_experts_forward / moe_infer); the
 // fused layer writes the sorted rows itself (RMSNorm scatter).  Either way the
-// rows are bf16 values, which two e4m3 terms hold.
+// rows are bf16 values, which two e4m3 terms hold (one dynamic-FP8 term under
+// that scheme).
 // plan_ready: the routing kernel has already written the workspace's inv_pos (the
 // inverse of sorted_pos) and tile list; otherwise they are derived here first.
 moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float* topk_weight,
@@ -306,19 +317,20 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
   float* xs_inv = at<float>(ws, L.xs_inv);
   TileDesc* tiles = at<TileDesc>(ws, L.tiles);
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
-  const int x_terms = 2;
+  const bool fp8 = fp8_act(d);
+  const int x_terms = x_terms_of(fp8);
   if (gather) {
     int32_t* ip = at<int32_t>(ws, L.inv_pos);
     if (!plan_ready) MOE_CHECK_CUDA(launch_invert_positions(sorted_pos, R, ip, s));
     MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), ip, static_cast<int32_t>(n), d->top_k, d->d,
-                                      xs, rows_layout(R, d->num_experts, d->d, x_terms), xs_inv, s));
+                                      xs, rows_layout(R, d->num_experts, d->d, x_terms, fp8), xs_inv, s));
     tr.after("gather_rows");
   }
   if (!plan_ready) {
     MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
     tr.after("build_tiles");
   }
-  return run_gemms(gather, w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
+  return run_gemms(gather, fp8, w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
                    at<float>(ws, L.h_inv), tiles, n_tiles, sorted_pos, topk_weight, rows, at<uint32_t>(ws, L.err), s,
                    tr, "gateup_swiglu", "down_scatter");
 }
@@ -330,7 +342,8 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles) + 1;
   MOE_CHECK_CUDA(launch_identity_tiles(static_cast<int32_t>(n), tile_tokens(n, 1), tiles, n_tiles, s));
   tr.after("shared_tiles");
-  return run_gemms(false, w, d->d, dff_sh, 1, static_cast<int32_t>(n), 2, at<uint8_t>(ws, L.xs_sh),
+  const bool fp8 = fp8_act(d);
+  return run_gemms(false, fp8, w, d->d, dff_sh, 1, static_cast<int32_t>(n), x_terms_of(fp8), at<uint8_t>(ws, L.xs_sh),
                    at<float>(ws, L.xs_sh_inv), at<uint8_t>(ws, L.h_sh), at<float>(ws, L.h_sh_inv), tiles, n_tiles,
                    nullptr, nullptr, at<uint16_t>(ws, L.sh_out), at<uint32_t>(ws, L.err), s, tr, "shared_gateup",
                    "shared_down");
@@ -539,8 +552,9 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
   const int64_t R = n * dims->top_k;
   MOE_CHECK_CUDA(launch_rmsnorm_scatter(
       static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(gain), eps, static_cast<int32_t>(n), dims->d,
-      dims->top_k, ip, at<uint8_t>(ws, L.xs), rows_layout(R, dims->num_experts, dims->d, 2), at<float>(ws, L.xs_inv),
-      shared ? at<uint8_t>(ws, L.xs_sh) : nullptr, rows_layout(n, 1, dims->d, 2),
+      dims->top_k, ip, at<uint8_t>(ws, L.xs),
+      rows_layout(R, dims->num_experts, dims->d, x_terms_of(fp8_act(dims)), fp8_act(dims)), at<float>(ws, L.xs_inv),
+      shared ? at<uint8_t>(ws, L.xs_sh) : nullptr, rows_layout(n, 1, dims->d, x_terms_of(fp8_act(dims)), fp8_act(dims)),
       shared ? at<float>(ws, L.xs_sh_inv) : nullptr, s));
   tr.after("rmsnorm_scatter");
   void* rows = at<void>(ws, L.rows);

@@ -53,7 +53,7 @@ struct TileDesc {
 // Token tile widths of the grouped GEMMs.  Decode-like batches (a few rows per
 // expert) use 16-token tiles whose three activation terms sit side by side on
 // the MMA's N axis (N = 48); from 24 rows per expert on, tiles of up to 128
-// tokens with the terms stacked along K (N = tile rows rounded up to 16).
+// tokens on the MMA's M side with the terms stacked along K.
 constexpr int kNTokSmall = 16;
 constexpr int kNTokWide = 128;
 __host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
@@ -65,14 +65,18 @@ __host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
 //   16-token tiles: rows interleaved with their terms, [rows][3][K]
 //                   (row_stride 3K, term_stride K, 3 terms)
 //   wide tiles:     one plane per term, [terms][rows][K]
-//                   (row_stride K, term_stride rows * K, 2 or 3 terms)
+//                   (row_stride K, term_stride rows * K, 1 to 3 terms)
+// fp8 != 0: the dynamic FP8 scheme, one e4m3 term per value with the scale
+// amax / 448 per 128 columns (the 16-token layout keeps its three slots, the
+// second and third zero; wide tiles keep one plane).
 struct SplitLayout {
   int64_t row_stride;
   int64_t term_stride;
   int32_t terms;
+  int32_t fp8;
 };
-inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms) {
-  return wide ? SplitLayout{K, rows * K, terms} : SplitLayout{3 * K, K, 3};
+inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms, bool fp8) {
+  return wide ? SplitLayout{K, rows * K, fp8 ? 1 : terms, fp8 ? 1 : 0} : SplitLayout{3 * K, K, 3, fp8 ? 1 : 0};
 }
 
 // Launch with programmatic stream serialization when `overlap`: the kernel may
@@ -135,7 +139,8 @@ struct GemmLaunch {
   const CUtensorMap* act;       // 16-token tiles: 2-D map over [3 rows][K] e4m3, box 128 x 48
   const CUtensorMap* act_box;   // wide tiles: 3-D map over [terms][rows][K], box 128 x 128 rows x terms
   int32_t ntok;                 // token tile width (kNTokSmall or kNTokWide)
-  int32_t terms;                // wide tiles: activation terms (2 or 3)
+  int32_t terms;                // wide tiles: activation terms (1 to 3)
+  bool fp8;                     // dynamic FP8 activations: gate/up writes h as one e4m3 term, scale amax / 448
   // Tiled layout (moe_pack_weights): both weight blocks of a unit per K block, 32 KB,
   // consecutive K blocks contiguous; used instead of w0 / w1 when non-null.
   const uint8_t* w_tiled;
@@ -147,10 +152,10 @@ struct GemmLaunch {
   // A unit is one token tile times two weight blocks: gate/up pass = row block j
   // of w0 and of w1; down pass = row blocks 2j and 2j + 1 of w0.
   int32_t num_kb;               // K / 128
-  const float* act_inv;         // [num_kb][act_rows] 2^-s of each activation block
+  const float* act_inv;         // [num_kb][act_rows] factor of each activation block (2^-s, or the FP8 scale)
   int32_t act_rows;             // rows of the sorted activation matrix
   void* out;                    // gate/up: h codes (layout of the next pass); down: rows [.][n_nb*128] f16
-  float* out_inv;               // gate/up: [n_nb][act_rows] 2^-s of each h block
+  float* out_inv;               // gate/up: [n_nb][act_rows] factor of each h block
   const int32_t* sorted_pos;    // down: flat position of each sorted row (NULL = identity)
   const float* topk_weight;     // down: flat router weights (NULL = 1)
   uint32_t* err;

@@ -2,8 +2,9 @@
 //
 // gather_rows_kernel    - "Mixture of experts" page, moe_infer: sorted_tokens
 //                         = x[idxs // k]; each token's row is split once into
-//                         the e4m3 split format the GEMMs read (split3.cuh) and
-//                         written to all of its sorted positions.
+//                         the e4m3 split format the GEMMs read (split3.cuh), or
+//                         quantised to dynamic FP8, and written to all of its
+//                         sorted positions.
 // rmsnorm_scatter_kernel- "Input features" page, RMSNorm: fp32 mean of squares,
 //                         h / sqrt(mean + eps) cast to bf16, times the bf16 gain
 //                         in bf16; the normalised row is split once (two terms
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
       if (kb >= nkb) break;
       const float v[4] = {bf16_lo(w[i].x), bf16_hi(w[i].x), bf16_lo(w[i].y), bf16_hi(w[i].y)};
       uint32_t t1, t2, t3;
-      const float inv = warp_split_block(v, t1, t2, t3);
+      const float inv = lay.fp8 ? warp_fp8_block(v, t1, t2, t3) : warp_split_block(v, t1, t2, t3);
       for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
     }
   }
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
     v[2] = bf16_round(bf16_lo(g.y) * bf16_round(bf16_lo(w.y) * inv_rms));
     v[3] = bf16_round(bf16_hi(g.y) * bf16_round(bf16_hi(w.y) * inv_rms));
     uint32_t t1, t2, t3;
-    const float inv = warp_split_block(v, t1, t2, t3);
+    const float inv = lay.fp8 ? warp_fp8_block(v, t1, t2, t3) : warp_split_block(v, t1, t2, t3);
     for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
     if (xs_shared) warp_store_block(xs_shared, lay_shared, xs_shared_inv, n, t, kb, t1, t2, t3, inv, lane);
   }

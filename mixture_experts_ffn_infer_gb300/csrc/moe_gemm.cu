@@ -32,7 +32,9 @@
 //
 // After the last K block the epilogue writes, per valid token column,
 //   gate/up pass : h = silu(g) * u in the split format (one block scale per
-//                  row and 128 features, found with a max over the 4 warps)
+//                  row and 128 features, found with a max over the 4 warps),
+//                  or as one dynamic-FP8 term (scale amax / 448) with the
+//                  other two terms zero
 //   down pass    : f16(topk_weight * o) -> rows[flat position][feature], both blocks
 //
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag and
@@ -92,7 +94,8 @@ struct GemmArgs {
   const float* act_inv;     // [num_kb][act_rows]: 2^-s of each activation block
   int32_t act_rows;
   void* out;                // gate/up: h terms [3 act_rows][n_nb*128] e4m3; down: rows [.][n_nb*128] f16
-  float* out_inv;           // gate/up: [n_nb][act_rows] 2^-s of each h block
+  float* out_inv;           // gate/up: [n_nb][act_rows] factor of each h block
+  int32_t fp8;              // gate/up: h as one dynamic-FP8 term (scale amax / 448) instead of three
   const int32_t* sorted_pos;
   const float* topk_weight;
   uint32_t* err;
@@ -412,15 +415,22 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         for (int j = 0; j < NTOK; ++j) {
           if (j < td.n_valid) {
             const float m = fmaxf(fmaxf(rb[j], rb[NTOK + j]), fmaxf(rb[2 * NTOK + j], rb[3 * NTOK + j]));
-            const int sexp = split_exponent(m);
-            uint8_t t1, t2, t3;
-            split3(ldexpf(hv[j], sexp), t1, t2, t3);
+            uint8_t t1, t2 = 0, t3 = 0;
+            float factor;
+            if (a.fp8) {  // dynamic FP8: one term, scale amax / 448
+              factor = fp8_block_scale(m);
+              t1 = float_to_e4m3(__fdiv_rn(hv[j], factor));
+            } else {
+              const int sexp = split_exponent(m);
+              split3(ldexpf(hv[j], sexp), t1, t2, t3);
+              factor = ldexpf(1.0f, -sexp);
+            }
             const int64_t row = td.row_start + j;
             uint8_t* dst = hterm + (3 * row) * ld + un.nb0 * 128 + r;
             dst[0] = t1;
             dst[ld] = t2;
             dst[2 * ld] = t3;
-            if (r == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = ldexpf(1.0f, -sexp);
+            if (r == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = factor;
           }
         }
       } else {
@@ -469,6 +479,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   a.act_rows = g.act_rows;
   a.out = g.out;
   a.out_inv = g.out_inv;
+  a.fp8 = g.fp8 ? 1 : 0;
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;

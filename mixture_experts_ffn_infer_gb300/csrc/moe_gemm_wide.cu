@@ -41,7 +41,9 @@
 // At the end of a unit the gate/up epilogue forms h = silu(g) * u and writes
 // it as three term planes, one exponent per (token, 128 features) from the
 // maximum over both feature halves (their float exponents, exchanged as bytes); the down epilogue writes
-// f16(topk_weight * o) to the row's flat position.  Every wait is bounded; a
+// f16(topk_weight * o) to the row's flat position.  With dynamic FP8
+// activations (TX = 1: one term per value) the gate/up epilogue exchanges the
+// halves' maxima as floats and writes one plane of codes of h / s, s = amax / 448.  Every wait is bounded; a
 // wait that gives up raises the abort flag and the device error word, and
 // every role drains what it has in flight before the kernel returns.
 #include <cuda_fp16.h>
@@ -67,8 +69,9 @@ struct WideCfg {
   static constexpr int kWStage = 2 * kWTileBytes;          // both weight blocks of one K block
   static constexpr int kAStage = TX * kTileMax * 128;      // the activation box: terms x 128 rows
   static constexpr int kAOff = WST * kWStage;
-  static constexpr int kRedOff = kAOff + AST * kAStage;    // h block-maximum exponents [parity][half][128 tokens]
-  static constexpr int kRedBytes = 2 * 2 * kTileMax;
+  // h block maxima [parity][half][128 tokens]: float exponents as bytes, or (TX = 1) the floats
+  static constexpr int kRedOff = kAOff + AST * kAStage;
+  static constexpr int kRedBytes = 2 * 2 * kTileMax * (TX == 1 ? 4 : 1);
   static constexpr int kBarOff = kRedOff + kRedBytes;
   static constexpr int kNumBars = 2 * WST + 2 * AST + 2 * 2 + 2 + 1;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
@@ -426,6 +429,37 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           overflow |= !(fabsf(acc0[j]) <= 3.0e38f);
         }
         overflow &= valid;
+        const int64_t ld = static_cast<int64_t>(n_nb) * 128;
+        uint8_t* hp = static_cast<uint8_t*>(a.out) + row * ld + un.nb0 * 128 + hf * kHalfF;
+        if (TX == 1) {
+          // dynamic FP8: the scale needs the maximum itself, exchanged as a float
+          float* rf = reinterpret_cast<float*>(red) + (ui & 1) * 2 * kTileMax;
+          rf[hf * kTileMax + tok] = m;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(redbar(ui & 1));
+          ok = __all_sync(0xffffffffu, wait_bounded(redbar(ui & 1), (ui >> 1) & 1, abort_flag, a.err));
+          if (!ok) break;
+          if (valid) {
+            const float sc = fp8_block_scale(fmaxf(m, rf[(hf ^ 1) * kTileMax + tok]));
+#pragma unroll
+            for (int v = 0; v < kHalfF / 32; ++v) {
+              uint32_t t[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float* x4 = acc0 + 32 * v + 4 * i;
+                const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(x4[0], sc), __fdiv_rn(x4[1], sc)), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(x4[2], sc), __fdiv_rn(x4[3], sc)), __NV_SATFINITE, __NV_E4M3);
+                t[i] = lo | (hi << 16);
+              }
+              stg256(hp + 32 * v, t);
+            }
+            if (hf == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = sc;
+          }
+          if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(a.err, DEV_ERR_RANGE);
+          continue;
+        }
         // the biased float exponent of the maximum is all the block scale needs
         uint8_t* rb = red + (ui & 1) * 2 * kTileMax;
         const uint32_t code = __float_as_uint(m) >> 23;  // m >= 0: 0 for zero or subnormal, 255 for inf
@@ -439,8 +473,6 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           const uint32_t c = max(code, static_cast<uint32_t>(rb[(hf ^ 1) * kTileMax + tok]));
           const int sexp = (c == 0u || c == 255u) ? 0 : 134 - static_cast<int>(c);
           const float f1 = pow2i(sexp >> 1), f2 = pow2i(sexp - (sexp >> 1));  // both factors stay normal
-          const int64_t ld = static_cast<int64_t>(n_nb) * 128;
-          uint8_t* hp = static_cast<uint8_t*>(a.out) + row * ld + un.nb0 * 128 + hf * kHalfF;
 #pragma unroll
           for (int v = 0; v < kHalfF / 32; ++v) {
             uint32_t t1[8], t2[8], t3[8];
@@ -524,13 +556,16 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
 // Stages: three weight stages of 32 KB (both blocks of one K block) and
 // activation stages of terms x 16 KB (three of 32 KB for the two terms of the
 // bf16 features, two of 48 KB for the three terms of h); about 195 KB of
-// shared memory.
+// shared memory.  Dynamic FP8 (one term): four weight stages and four 16 KB
+// activation stages, the same shared memory.
 cudaError_t launch_gateup_wide(const GemmLaunch& g, cudaStream_t s) {
-  if (g.terms == 2) return launch_wide<true, 2, 3, 3>(g, s);
+  if (g.terms == 2 && !g.fp8) return launch_wide<true, 2, 3, 3>(g, s);
+  if (g.terms == 1 && g.fp8) return launch_wide<true, 1, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down_wide(const GemmLaunch& g, cudaStream_t s) {
-  if (g.terms == 3) return launch_wide<false, 3, 3, 2>(g, s);
+  if (g.terms == 3 && !g.fp8) return launch_wide<false, 3, 3, 2>(g, s);
+  if (g.terms == 1 && g.fp8) return launch_wide<false, 1, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 

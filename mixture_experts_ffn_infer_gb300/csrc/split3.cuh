@@ -10,7 +10,8 @@
 // range stays inside e4m3's (so bf16 rows are stored as two terms); the third
 // term carries an fp32 intermediate (h) to about 12 bits.  The GEMMs sum the
 // terms' partial products - in the epilogue for 16-token tiles, in the tensor
-// core's accumulator for wide tiles - and multiply by 2^-s in fp32.
+// core's accumulator for wide tiles - and multiply by 2^-s in fp32.  The
+// dynamic FP8 scheme below uses the same storage with a single term.
 #pragma once
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -94,15 +95,38 @@ __device__ __forceinline__ float warp_split_block(const float (&v)[4], uint32_t&
   return ldexpf(1.0f, -s);
 }
 
-// Store a block converted by warp_split_block for sorted row `row` at column
-// block kb: the codes go where `lay` puts them (the third term only when the
-// layout keeps three), the exponent to inv[kb * n_rows + row].
+// Dynamic FP8 activations ("Input features" page, quantisation config:
+// activation_scheme "dynamic", fmt e4m3): one e4m3 term per value, with the
+// scale s = amax / 448 of its 128-column block (1 for an all-zero block),
+// code = nearest e4m3 of v / s with ties to even and saturation at 448.  The
+// divisions are IEEE round-to-nearest, so a bf16 input's codes are exactly
+// reproducible.
+__device__ __forceinline__ float fp8_block_scale(float amax) {
+  const float s = __fdiv_rn(amax, 448.0f);
+  return s > 0.f ? s : 1.0f;
+}
+
+// One warp, one 128-column block, lane l holding columns 4l..4l+3: t1 gets the
+// lane's four codes, t2 and t3 zero; returns the block scale.
+__device__ __forceinline__ float warp_fp8_block(const float (&v)[4], uint32_t& t1, uint32_t& t2, uint32_t& t3) {
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  const float s = fp8_block_scale(warp_max(m));
+  t1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t1 |= static_cast<uint32_t>(float_to_e4m3(__fdiv_rn(v[i], s))) << (8 * i);
+  t2 = t3 = 0;
+  return s;
+}
+
+// Store a block converted by warp_split_block or warp_fp8_block for sorted
+// row `row` at column block kb: the codes go where `lay` puts them (as many
+// terms as the layout keeps), the block's factor to inv[kb * n_rows + row].
 __device__ __forceinline__ void warp_store_block(uint8_t* codes, SplitLayout lay, float* inv, int64_t n_rows,
                                                  int64_t row, int kb, uint32_t t1, uint32_t t2, uint32_t t3,
                                                  float inv_s, int lane) {
   uint8_t* base = codes + row * lay.row_stride + static_cast<int64_t>(kb) * 128;
   reinterpret_cast<uint32_t*>(base)[lane] = t1;
-  reinterpret_cast<uint32_t*>(base + lay.term_stride)[lane] = t2;
+  if (lay.terms > 1) reinterpret_cast<uint32_t*>(base + lay.term_stride)[lane] = t2;
   if (lay.terms > 2) reinterpret_cast<uint32_t*>(base + 2 * lay.term_stride)[lane] = t3;
   if (lane == 0) inv[static_cast<int64_t>(kb) * n_rows + row] = inv_s;
 }

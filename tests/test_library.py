@@ -59,6 +59,11 @@ def test_workspace_size_rules(lib):
     assert mx.moe_workspace_size(mx.dims(7168, 2048, 384, 33), 16) == 0          # k too large
     assert mx.moe_workspace_size(mx.dims(7168, 2048, 384, 8), 1 << 29) == 0     # n*k >= 2^31
     assert mx.moe_workspace_size(dm, 16, 100) == 0                              # shared width not x128
+    # the activation scheme: dynamic FP8 uses the same workspace; unknown schemes are unsupported
+    fp8 = mx.dims(7168, 2048, 384, 8, mx.MOE_ACT_FP8_DYNAMIC)
+    assert mx.moe_workspace_size(fp8, 4096, 2048) == c
+    for bad in (2, -1):
+        assert mx.moe_workspace_size(mx.dims(7168, 2048, 384, 8, bad), 16) == 0
 
 
 def test_host_argument_errors_return_codes_without_a_device(lib):
