@@ -276,6 +276,10 @@ moe_status run_gemms(bool after_gather, bool fp8, const moe_weights* w, int64_t 
   g.err = err;
   g.num_sms = num_sms();
   g.overlap = after_gather;
+  // Wide tiles: the L2 prefetch ahead of the weight copies pays when an expert's
+  // weights serve several token tiles (measured: -1.5 % at one tile per expert,
+  // +1 to +4 % with several), so it is on from one full tile per expert.
+  g.l2_prefetch = static_cast<int64_t>(rows) >= static_cast<int64_t>(kNTokWide) * experts;
   if (g.num_sms <= 0) return MOE_ERR_CUDA;
   tr.before_gemm();
   MOE_CHECK_CUDA(launch_gateup(g, s));

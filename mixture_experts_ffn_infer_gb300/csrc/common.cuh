@@ -161,6 +161,7 @@ struct GemmLaunch {
   uint32_t* err;
   int num_sms;
   bool overlap;                 // gate/up: launched behind the row gather (dependent launch)
+  bool l2_prefetch;             // wide tiles: prefetch weights into L2 ahead of their copies
 };
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s);

@@ -89,6 +89,7 @@ struct WideArgs {
   int32_t n_nb;             // 128-row blocks of the weight matrix
   int32_t num_kb;           // K / 128
   int32_t pair;             // 1: unit = row blocks 2j, 2j+1 of w0 (down); 0: row block j of w0 and w1
+  int32_t l2_prefetch;      // prefetch weights into L2 ahead of their copies
   const float* act_inv;     // [num_kb][act_rows]
   int32_t act_rows;
   void* out;                // gate/up: h term planes [3][act_rows][n_nb*128]; down: rows [.][n_nb*128] f16
@@ -246,7 +247,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       int pf_u = blockIdx.x, pf_kb = 0;
       Unit pf{};
       auto prefetch_one = [&]() {
-        if (pf_u >= total_units) return;
+        if (!a.l2_prefetch || pf_u >= total_units) return;
         if (pf_kb == 0) pf = unit_of(a, pf_u, upt);
         if (a.w_tiled) {
           bulk_prefetch_l2(a.w_tiled + unit_off(pf.e, pf.ru, pf_kb), 2 * kWTileBytes);
@@ -538,6 +539,7 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
   a.n_nb = g.n_nb;
   a.num_kb = g.num_kb;
   a.pair = GATEUP ? 0 : 1;
+  a.l2_prefetch = g.l2_prefetch ? 1 : 0;
   a.act_inv = g.act_inv;
   a.act_rows = g.act_rows;
   a.out = g.out;
