@@ -228,6 +228,24 @@ moe_status moe_layer_forward(const moe_dims *dims, int64_t n_tokens, const void 
                              void *out, int32_t out_is_fp32, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream, moe_trace *trace);
 
+/* One SwiGLU MLP on every row ("SwiGLU output" page, MLP class: the same
+ * module as each expert, which the model's dense feed-forward blocks also
+ * use; their width is not printed on the pages, so d_ff is the caller's):
+ *   out[t] = down( silu(gate x[t]) * up x[t] )
+ * run through the same gather and grouped-GEMM kernels as a single expert
+ * segment that holds all n rows in order, with weight 1.
+ *   dims      num_experts = 1, top_k = 1 (else MOE_ERR_UNSUPPORTED); d_ff is
+ *             the MLP's width; act_scheme as for moe_infer
+ *   x         [n, d] bf16 in
+ *   weights   one bank with E = 1 (either layout)
+ *   out       [n, d] bf16, or fp32 when out_is_fp32 != 0
+ *   workspace moe_workspace_size(dims, n, 0) bytes
+ * Device-detected errors (f16 overflow, a timeout) accumulate in the
+ * workspace's error word until moe_get_error reads it. */
+moe_status moe_mlp_forward(const moe_dims *dims, int64_t n_tokens, const void *x, const moe_weights *weights,
+                           void *out, int32_t out_is_fp32, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
 /* moe_infer without a workspace, for callers that cannot allocate device
  * memory themselves: code that only receives input and output buffers from a
  * host framework (a plugin or an embedded runtime with its own memory

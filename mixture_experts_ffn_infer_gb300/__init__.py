@@ -84,6 +84,9 @@ _SIGS = {
                                          ctypes.POINTER(moe_weights), ctypes.POINTER(moe_weights), ctypes.c_int32,
                                          ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
                                          ctypes.c_void_p, ctypes.POINTER(moe_trace)]),
+    "moe_mlp_forward": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64, ctypes.c_void_p,
+                                       ctypes.POINTER(moe_weights), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                       ctypes.c_size_t, ctypes.c_void_p]),
     "moe_infer_static": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 3
                          + [ctypes.POINTER(moe_weights), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "moe_check_bounded_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
@@ -199,6 +202,13 @@ def moe_infer(dm, n_tokens, x, topk_ids, topk_weight, w: moe_weights, out, ws, o
     _check(st, "moe_infer")
 
 
+def moe_mlp_forward(dm, n_tokens, x, w: moe_weights, out, ws, out_is_fp32=False, stream=None):
+    st = load_library().moe_mlp_forward(ctypes.byref(dm), n_tokens, _ptr(x), ctypes.byref(w), _ptr(out),
+                                        int(bool(out_is_fp32)), _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream))
+    _check(st, "moe_mlp_forward")
+
+
 def moe_layer_forward(dm, n_tokens, hidden, gain, eps, topk_ids, topk_weight, routed: moe_weights,
                       shared: Optional[moe_weights], d_ff_shared, out, ws, out_is_fp32=False, stream=None,
                       trace: Optional[moe_trace] = None):
@@ -296,6 +306,19 @@ def infer(x, topk_ids, topk_weight, bank, ws=None, out_is_fp32=False, stream=Non
         ws = workspace(dm, n, 0, x.device)
     out = torch.empty(n, d, dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=x.device)
     moe_infer(dm, n, x, topk_ids, topk_weight, weights(bank), out, ws, out_is_fp32, stream)
+    return out
+
+
+def mlp_forward(x, bank, ws=None, out_is_fp32=False, stream=None, act_scheme=MOE_ACT_EXACT):
+    """One SwiGLU MLP (a bank with E = 1) on every row of x."""
+    import torch
+    n, d = x.shape
+    E, d_ff, _ = bank_sizes(bank)
+    dm = moe_dims(d, d_ff, E, 1, act_scheme)
+    if ws is None:
+        ws = workspace(dm, n, 0, x.device)
+    out = torch.empty(n, d, dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=x.device)
+    moe_mlp_forward(dm, n, x, weights(bank), out, ws, out_is_fp32, stream)
     return out
 
 

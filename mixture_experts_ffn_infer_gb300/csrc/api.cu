@@ -575,6 +575,36 @@ moe_status moe_layer_forward(const moe_dims* dims, int64_t n, const void* hidden
   return MOE_OK;
 }
 
+moe_status moe_mlp_forward(const moe_dims* dims, int64_t n, const void* x, const moe_weights* w, void* out,
+                           int32_t out_is_fp32, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
+  if (dims->num_experts != 1 || dims->top_k != 1) return MOE_ERR_UNSUPPORTED;
+  Layout L;
+  if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (n == 0) return MOE_OK;
+  if (!x || !out || !weights_ok(w) || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = fp8_act(dims);
+  const int32_t R = static_cast<int32_t>(n);
+  TileDesc* tiles = at<TileDesc>(ws, L.tiles);
+  int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
+  uint8_t* xs = at<uint8_t>(ws, L.xs);
+  float* xs_inv = at<float>(ws, L.xs_inv);
+  Tracer tr{nullptr, s};
+  // all n rows form one segment in their own order: identity tiles, identity gather
+  MOE_CHECK_CUDA(launch_identity_tiles(R, tile_tokens(R, 1), tiles, n_tiles, s));
+  MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), nullptr, R, 1, dims->d, xs,
+                                    rows_layout(R, 1, dims->d, x_terms_of(fp8), fp8), xs_inv, s));
+  void* rows = at<void>(ws, L.rows);
+  moe_status st = run_gemms(true, fp8, w, dims->d, dims->d_ff, 1, R, x_terms_of(fp8), xs, xs_inv,
+                            at<uint8_t>(ws, L.h), at<float>(ws, L.h_inv), tiles, n_tiles, nullptr, nullptr, rows,
+                            at<uint32_t>(ws, L.err), s, tr, "mlp_gateup", "mlp_down");
+  if (st != MOE_OK) return st;
+  MOE_CHECK_CUDA(launch_combine(static_cast<const uint16_t*>(rows), nullptr, nullptr, R, 1, dims->d, out,
+                                out_is_fp32, s));
+  return MOE_OK;
+}
+
 moe_status moe_infer_static(const moe_dims* dims, int64_t n, const void* x, const int32_t* topk_ids,
                             const float* topk_weight, const moe_weights* w, void* out, int32_t out_is_fp32,
                             cudaStream_t s) {

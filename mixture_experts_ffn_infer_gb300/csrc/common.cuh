@@ -114,7 +114,8 @@ cudaError_t launch_identity_tiles(int32_t rows, int32_t ntok, TileDesc* tiles, i
 
 // elementwise.cu
 // Sorted activation rows in the split format from the bf16 tokens: inv_pos [n k]
-// gives each routed slot's sorted position (-1: none).
+// gives each routed slot's sorted position (-1: none; a null inv_pos keeps the
+// slots' own order, position t k + j).
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* inv_pos, int32_t n, int32_t k, int32_t d,
                                uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s);
 // inv_pos from sorted_pos (entries that no sorted row names become -1).

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
   int32_t dst_rows[32];
   int ndst = 0;
   for (int j = 0; j < k; ++j) {
-    const int p = inv_pos[t * k + j];
+    const int p = inv_pos ? inv_pos[t * k + j] : static_cast<int>(t * k + j);  // null: identity order
     if (p >= 0 && p < R) dst_rows[ndst++] = p;
   }
   if (ndst == 0) return;

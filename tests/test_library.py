@@ -93,6 +93,15 @@ def test_host_argument_errors_return_codes_without_a_device(lib):
                                0, None, 0, ctypes.c_void_p(addr), 1 << 30, None, None) == 1
     assert L.moe_combine(ctypes.byref(dm), 8, None, None, None, None, 0, None) == 1
     assert L.moe_get_error(None, None) == 1
+    # the MLP entry point takes one expert and k = 1 only, then checks like moe_infer
+    one = mx.dims(1024, 256, 1, 1)
+    assert L.moe_mlp_forward(ctypes.byref(dm), 8, None, ctypes.byref(w), None, 0, ctypes.c_void_p(addr), 1 << 30,
+                             None) == 2
+    assert L.moe_mlp_forward(ctypes.byref(one), 8, None, ctypes.byref(w), None, 0, None, 0, None) == 3
+    assert L.moe_mlp_forward(ctypes.byref(one), 8, None, ctypes.byref(w), None, 0, ctypes.c_void_p(addr), 1 << 30,
+                             None) == 1
+    assert L.moe_mlp_forward(ctypes.byref(one), 0, None, ctypes.byref(w), None, 0, ctypes.c_void_p(addr), 1 << 30,
+                             None) == 0
 
 
 def test_tiled_bytes_and_permute_workspace(lib):
