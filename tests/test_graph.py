@@ -66,3 +66,38 @@ def test_layer_graph_replay_matches_eager():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("act", [mx.MOE_ACT_EXACT, mx.MOE_ACT_FP8_DYNAMIC])
+def test_mlp_and_fp8_infer_graph_replay_matches_eager(act):
+    # the dense MLP entry point (wide tiles) and moe_infer in either activation scheme, in one graph
+    c = cases.workload(syn.Workload("gf", 200, 512, 256, 8, 2, seed=23))
+    n, d = c.x.shape
+    dm = mx.dims(d, 256, 8, 2, act)
+    dm1 = mx.dims(d, 256, 1, 1, act)
+    mlp_bank = syn.ExpertBank(*(t[:1].contiguous() for t in (c.bank.w_gate, c.bank.w_up, c.bank.w_down,
+                                                              c.bank.s_gate, c.bank.s_up, c.bank.s_down)))
+    ws, ws1 = mx.workspace(dm, n), mx.workspace(dm1, n)
+    W, W1 = mx.weights(c.bank), mx.weights(mlp_bank)
+    out = torch.empty(n, d, dtype=torch.bfloat16, device="cuda")
+    out1 = torch.empty(n, d, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+
+    def body():
+        mx.moe_infer(dm, n, c.x, c.ids, c.w, W, out, ws, stream=s)
+        mx.moe_mlp_forward(dm1, n, c.x, W1, out1, ws1, stream=s)
+
+    with torch.cuda.stream(s):
+        body()
+    s.synchronize()
+    eager, eager1 = out.clone(), out1.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        body()
+    out.zero_()
+    out1.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager) and torch.equal(out1, eager1)
+    assert mx.moe_get_error(ws) == mx.MOE_OK and mx.moe_get_error(ws1) == mx.MOE_OK
