@@ -170,3 +170,43 @@ def test_k2_block_sampled_tokens():
                                c.shared, tokens=tok)
     _assert_ok(y[tok], ref)
     assert torch.isfinite(y.float()).all()
+
+
+def _hot_expert_rows(c, act=mx.MOE_ACT_EXACT):
+    """moe_permute + moe_experts_forward on the tiled bank; returns (rows f16 [n, k, d] on the GPU,
+    the hottest expert, its (token, slot) entries at the first and last valid row of every 128-row tile)."""
+    n, k = c.ids.shape
+    E, d_ff, d = 384, 2048, 7168
+    dm = mx.dims(d, d_ff, E, k, act)
+    ws = mx.workspace(dm, n)
+    counts, offsets, sp, ip = mx.permute(c.ids, E, ws=ws)
+    bank_t = mx.pack_bank(c.bank)
+    torch.cuda.synchronize()
+    rows = torch.empty(n, k, d, dtype=torch.float16, device="cuda")
+    mx.moe_experts_forward(dm, n, c.x, c.w, offsets, sp, mx.weights(bank_t), rows, ws)
+    torch.cuda.synchronize()
+    assert mx.moe_get_error(ws) == mx.MOE_OK
+    del bank_t
+    counts, offsets, sp = counts.cpu(), offsets.cpu(), sp.cpu()
+    hot = int(counts.argmax())
+    lo, cnt = int(offsets[hot]), int(counts[hot])
+    picks = sorted({i for t0 in range(0, cnt, 128) for i in (t0, min(t0 + 127, cnt - 1))})
+    entries = [(int(sp[lo + i]) // k, int(sp[lo + i]) % k) for i in picks]
+    return rows, hot, entries
+
+
+def test_k2_skewed_hot_expert_every_tile():
+    # the skewed workload's hottest expert spans about sixty 128-row tiles of one expert (wide kernel,
+    # several tiles per expert, a ragged last tile): its first and last row of every tile against the oracle
+    c = cases.workload("k2_skewed")
+    rows, hot, entries = _hot_expert_rows(c)
+    assert len(entries) >= 100
+    b = c.bank
+    W = [t[hot].cpu() for t in (b.w_gate, b.s_gate, b.w_up, b.s_up, b.w_down, b.s_down)]
+    xt = torch.stack([c.inp.x[t] for t, _ in entries]).double().numpy()
+    o = oracle.expert_forward(xt, *W)
+    for i, (t, j) in enumerate(entries):
+        ref = o[i] * float(c.inp.topk_weight[t, j])
+        got = rows[t, j].double().cpu().numpy()
+        rms = np.sqrt(np.mean(ref ** 2))
+        assert np.max(np.abs(got - ref) - 2.0 ** -10 * np.abs(ref)) <= 1e-2 * rms, (t, j)

@@ -121,3 +121,18 @@ def test_k2_block_fp8_sampled_tokens():
                                c.shared, tokens=tok, fp8_act=True)
     _assert_ok(y[tok], ref)
     assert torch.isfinite(y.float()).all()
+
+
+def test_k2_skewed_hot_expert_every_tile_fp8():
+    from tests.test_parity import _hot_expert_rows
+    c = cases.workload("k2_skewed")
+    rows, hot, entries = _hot_expert_rows(c, FP8)
+    b = c.bank
+    W = [t[hot].cpu() for t in (b.w_gate, b.s_gate, b.w_up, b.s_up, b.w_down, b.s_down)]
+    xt = torch.stack([c.inp.x[t] for t, _ in entries]).double().numpy()
+    o = oracle.expert_forward(xt, *W, fp8_act=True)
+    for i, (t, j) in enumerate(entries):
+        ref = o[i] * float(c.inp.topk_weight[t, j])
+        got = rows[t, j].double().cpu().numpy()
+        rms = np.sqrt(np.mean(ref ** 2))
+        assert np.max(np.abs(got - ref) - 2.0 ** -10 * np.abs(ref)) <= 1e-2 * rms, (t, j)
