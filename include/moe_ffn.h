@@ -122,8 +122,10 @@ typedef struct {
 /* Optional per-kernel timing.  The caller creates up to MOE_TRACE_MAX events;
  * a call that receives a trace records events[0] before its first kernel and
  * events[i + 1] after its i-th kernel on `stream`, sets labels[i] to a static
- * name for that kernel and n_recorded to the number of events recorded.  Pass
- * NULL to record nothing. */
+ * name for that kernel and n_recorded to the number of events recorded.  With
+ * n_events = 0 nothing is recorded but n_launched is still set.  Pass NULL to
+ * record and count nothing.  An event between two kernels costs the stream
+ * about a launch gap, so timing a sample of calls disturbs the rest least. */
 #define MOE_TRACE_MAX 16
 typedef struct {
     cudaEvent_t events[MOE_TRACE_MAX];
