@@ -45,9 +45,11 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
 
 constexpr int kRowThreads = 256;  // eight warps per row, one 128-column block per warp at a time
 
-// One CTA per token: the token's row is read once, each 128-column block is
-// split once and written to every sorted position of the token (inv_pos).
-// Each warp keeps four blocks' loads in flight before it converts them.
+// One CTA per token and column group (blockIdx.y of gridDim.y, a batch with
+// fewer tokens than SMs spreads each row over several CTAs): the token's row is
+// read once, each 128-column block is split once and written to every sorted
+// position of the token (inv_pos).  Each warp keeps four blocks' loads in
+// flight before it converts them.
 __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                                   const int32_t* __restrict__ inv_pos, int32_t n,
                                                                   int32_t k, int32_t d, uint8_t* __restrict__ xs,
@@ -67,16 +69,17 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
   const uint2* src = reinterpret_cast<const uint2*>(x + t * d);
   const int nkb = d / 128;
   constexpr int kWarps = kRowThreads / 32, kBatch = 4;
-  for (int kb0 = warp; kb0 < nkb; kb0 += kWarps * kBatch) {
+  const int step = kWarps * static_cast<int>(gridDim.y);  // column blocks apart of one warp's consecutive blocks
+  for (int kb0 = static_cast<int>(blockIdx.y) * kWarps + warp; kb0 < nkb; kb0 += step * kBatch) {
     uint2 w[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      const int kb = kb0 + kWarps * i;
+      const int kb = kb0 + step * i;
       w[i] = kb < nkb ? src[kb * 32 + lane] : make_uint2(0u, 0u);
     }
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      const int kb = kb0 + kWarps * i;
+      const int kb = kb0 + step * i;
       if (kb >= nkb) break;
       const float v[4] = {bf16_lo(w[i].x), bf16_hi(w[i].x), bf16_lo(w[i].y), bf16_hi(w[i].y)};
       uint32_t t1, t2, t3;
@@ -249,7 +252,15 @@ cudaError_t launch_pack_tiles(const uint8_t* src0, const uint8_t* src1, uint8_t*
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* inv_pos, int32_t n, int32_t k, int32_t d,
                                uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  gather_rows_kernel<<<n, kRowThreads, 0, s>>>(x_bf16, inv_pos, n, k, d, xs, lay, xs_inv);
+  // a batch smaller than the GPU spreads each row's column blocks over several CTAs
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    sms = 1;
+  const int nkb = d / 128;
+  const int max_groups = (nkb + kRowThreads / 32 - 1) / (kRowThreads / 32);
+  const int groups = n >= sms ? 1 : max(1, min(max_groups, sms / n));
+  gather_rows_kernel<<<dim3(n, groups), kRowThreads, 0, s>>>(x_bf16, inv_pos, n, k, d, xs, lay, xs_inv);
   return cudaGetLastError();
 }
 
