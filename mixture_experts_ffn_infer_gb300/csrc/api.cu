@@ -117,16 +117,18 @@ bool map_weights(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Split-format codes of `rows` sorted rows: [3 rows][K] e4m3, box 128 (K) x 3 ntok
-// (three terms of ntok rows), 128-byte swizzle; rows past the end read as zero.
-bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, int ntok) {
+// Split-format codes of `rows` sorted rows, rows interleaved with their three
+// term slots: [rows][3][K] e4m3.  Box 128 (K) x `terms` slots x ntok rows, so
+// only the live terms are loaded (smem order [row][term][128 B]), 128-byte
+// swizzle; rows past the end read as zero.
+bool map_act(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, int terms, int ntok) {
   EncodeFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {K, 3 * rows};
-  const cuuint64_t strides[1] = {K};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(3 * ntok)};
-  const cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+  const cuuint64_t dims[3] = {K, 3, rows};
+  const cuuint64_t strides[2] = {K, 3 * K};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(terms), static_cast<cuuint32_t>(ntok)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -225,7 +227,7 @@ struct ActMaps {
   CUtensorMap m16;
   CUtensorMap box;
   bool make(bool wide, const void* base, uint64_t K, uint64_t rows, int terms) {
-    if (!wide) return map_act(&m16, base, K, rows, kNTokSmall);
+    if (!wide) return map_act(&m16, base, K, rows, terms, kNTokSmall);
     if (!map_act_planar(&box, base, K, rows, terms, kNTokWide)) return false;
     m16 = box;
     return true;

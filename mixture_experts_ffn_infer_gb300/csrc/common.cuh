@@ -62,13 +62,13 @@ __host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
 
 // Where the split-format codes of a sorted row live (split3.cuh): term t of
 // row i starts at base + i * row_stride + t * term_stride bytes.
-//   16-token tiles: rows interleaved with their terms, [rows][3][K]
-//                   (row_stride 3K, term_stride K, 3 terms)
+//   16-token tiles: rows interleaved with three term slots, [rows][3][K]
+//                   (row_stride 3K, term_stride K; the live terms first)
 //   wide tiles:     one plane per term, [terms][rows][K]
 //                   (row_stride K, term_stride rows * K, 1 to 3 terms)
 // fp8 != 0: the dynamic FP8 scheme, one e4m3 term per value with the scale
-// amax / 448 per 128 columns (the 16-token layout keeps its three slots, the
-// second and third zero; wide tiles keep one plane).
+// amax / 448 per 128 columns (the first slot of the 16-token layout, or one
+// plane of the wide layout).
 struct SplitLayout {
   int64_t row_stride;
   int64_t term_stride;
@@ -76,7 +76,7 @@ struct SplitLayout {
   int32_t fp8;
 };
 inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms, bool fp8) {
-  return wide ? SplitLayout{K, rows * K, fp8 ? 1 : terms, fp8 ? 1 : 0} : SplitLayout{3 * K, K, 3, fp8 ? 1 : 0};
+  return wide ? SplitLayout{K, rows * K, fp8 ? 1 : terms, fp8 ? 1 : 0} : SplitLayout{3 * K, K, fp8 ? 1 : terms, fp8 ? 1 : 0};
 }
 
 // Launch with programmatic stream serialization when `overlap`: the kernel may
@@ -137,10 +137,10 @@ struct GemmLaunch {
   // weights: 3-D maps over [E][rows][K] e4m3, box 128 x 128 x 1, 128-byte swizzle
   const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
   const CUtensorMap* w1;        // up (gate/up pass only)
-  const CUtensorMap* act;       // 16-token tiles: 2-D map over [3 rows][K] e4m3, box 128 x 48
+  const CUtensorMap* act;       // 16-token tiles: 3-D map over [rows][3][K] e4m3, box 128 x terms x 16
   const CUtensorMap* act_box;   // wide tiles: 3-D map over [terms][rows][K], box 128 x 128 rows x terms
   int32_t ntok;                 // token tile width (kNTokSmall or kNTokWide)
-  int32_t terms;                // wide tiles: activation terms (1 to 3)
+  int32_t terms;                // live activation terms per row (1 to 3)
   bool fp8;                     // dynamic FP8 activations: gate/up writes h as one e4m3 term, scale amax / 448
   // Tiled layout (moe_pack_weights): both weight blocks of a unit per K block, 32 KB,
   // consecutive K blocks contiguous; used instead of w0 / w1 when non-null.

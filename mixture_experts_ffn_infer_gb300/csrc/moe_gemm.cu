@@ -16,14 +16,16 @@
 // global memory to shared memory by bulk copy (tiled layout: both blocks of
 // KPS consecutive K blocks in one copy) or TMA (row-major layout) and
 // straight into tcgen05.mma kind::f8f6f4 - no conversion.  The activations
-// arrive in the three-term e4m3 split format (split3.cuh): the N side of each
-// MMA holds the three terms of NTOK tokens (N = 3 NTOK).  Per 128-wide K block:
+// arrive in the e4m3 split format (split3.cuh), rows interleaved with three
+// term slots; the N side of each MMA holds the TT live terms of NTOK tokens
+// (N = TT NTOK): two for the bf16 features of gate/up, three for h in down,
+// one for either under the dynamic FP8 scheme.  Per 128-wide K block:
 //
 //   warp 0      weight producer: stages of KPS K blocks x both weight blocks
 //               into a ring.
-//   warp 2      activation producer: the block of 3 NTOK rows x 128 bytes
+//   warp 2      activation producer: a 3-D box of NTOK rows x TT terms x 128 bytes
 //               into its own ring, so neither ring throttles the other.
-//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=3 NTOK, K=32) per
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=TT NTOK, K=32) per
 //               weight block into a fresh fp32 partial in tensor memory.
 //   warps 4-7   epilogue: per token, sum the three term columns, multiply by
 //               the weight block's fp32 scale and the activation block's 2^-s
@@ -61,10 +63,11 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int NTOK, int KPS, int WST, int BST, int DST>
+template <int NTOK, int TT, int KPS, int WST, int BST, int DST>
 struct Cfg {
   static_assert(NTOK <= 32, "one token per lane for the activation exponents");
-  static constexpr int kNB = 3 * NTOK;                   // MMA N: three e4m3 terms per token
+  static_assert(TT >= 1 && TT <= 3, "one to three e4m3 terms per token");
+  static constexpr int kNB = TT * NTOK;                  // MMA N: the live e4m3 terms of every token
   static constexpr int kWTile = 128 * 128;               // e4m3 weight tile bytes
   static constexpr int kWKb = 2 * kWTile;                // both weight blocks of one K block
   static constexpr int kWStage = KPS * kWKb;             // one weight stage: [K block][block][tile]
@@ -133,11 +136,11 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-template <bool GATEUP, int NTOK, int KPS, int WST, int BST, int DST>
+template <bool GATEUP, int NTOK, int TT, int KPS, int WST, int BST, int DST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                 const __grid_constant__ CUtensorMap tm_act, const GemmArgs a) {
-  using C = Cfg<NTOK, KPS, WST, BST, DST>;
+  using C = Cfg<NTOK, TT, KPS, WST, BST, DST>;
   constexpr int NB = C::kNB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -258,7 +261,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
           }
           const uint32_t bst = sbase + C::kBOffset + sb * C::kBStage;
           mbar_arrive_expect_tx(full_b(sb), C::kBStage);
-          tma_load_2d(bst, &tm_act, full_b(sb), kb * 128, row0 * 3, pol_a);
+          tma_load_3d(bst, &tm_act, full_b(sb), kb * 128, 0, row0, pol_a);  // [NTOK rows][TT terms][128 B]
           ++b_issued;
         }
       }
@@ -362,7 +365,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NTOK / 16; ++c) {  // 16 tokens (48 tensor-memory columns) at a time
+        for (int c = 0; c < NTOK / 16; ++c) {  // 16 tokens (16 TT tensor-memory columns) at a time
           float sx[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) sx[j] = __shfl_sync(0xffffffffu, sx_lane, 16 * c + j);
@@ -370,16 +373,17 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
           for (int m = 0; m < 2; ++m) {
             if (m == 1 && !un.has1) break;
             const float sv = m == 0 ? s0v : s1v;
-            uint32_t p[48];
+            uint32_t p[16 * TT];
 #pragma unroll
-            for (int c0 = 0; c0 < 48; c0 += 16)
-              tmem_ld16(tmem + lane_base + (sd * 2 + m) * NB + 48 * c + c0,
+            for (int c0 = 0; c0 < 16 * TT; c0 += 16)
+              tmem_ld16(tmem + lane_base + (sd * 2 + m) * NB + 16 * TT * c + c0,
                         *reinterpret_cast<uint32_t(*)[16]>(&p[c0]));
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float part = (__uint_as_float(p[3 * j]) + __uint_as_float(p[3 * j + 1])) +
-                                 __uint_as_float(p[3 * j + 2]);
+              float part = __uint_as_float(p[TT * j]);  // the token's terms, first to last
+#pragma unroll
+              for (int t = 1; t < TT; ++t) part += __uint_as_float(p[TT * j + t]);
               acc[m][16 * c + j] = fmaf(sv * sx[j], part, acc[m][16 * c + j]);
             }
           }
@@ -460,10 +464,10 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   }
 }
 
-template <bool GATEUP, int NTOK, int KPS, int WST, int BST, int DST>
+template <bool GATEUP, int NTOK, int TT, int KPS, int WST, int BST, int DST>
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  using C = Cfg<NTOK, KPS, WST, BST, DST>;
-  auto kern = moe_gemm_kernel<GATEUP, NTOK, KPS, WST, BST, DST>;
+  using C = Cfg<NTOK, TT, KPS, WST, BST, DST>;
+  auto kern = moe_gemm_kernel<GATEUP, NTOK, TT, KPS, WST, BST, DST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   GemmArgs a;
@@ -495,20 +499,25 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 // completes at a roughly fixed number of copy groups per memory round trip, so
 // the bytes per stage set the bandwidth (a probe streaming into shared memory
 // reached 7.0 TB/s with 64 KB stages and 2.0 TB/s with 16 KB stages).
-// Decode-sized tiles (16 tokens, MMA N = 48):
-//   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 x 6 KB activation stages,
-//            4 partial buffers (384 tensor-memory columns)
-//   down:    3 stages of 2 K blocks x 2 row blocks = 64 KB, 4 x 6 KB activation stages,
+// Decode-sized tiles (16 tokens; MMA N = 16 per live term: 32 for the two terms
+// of gate/up's bf16 features, 48 for h's three in down, 16 under dynamic FP8):
+//   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 activation stages of
+//            2 KB per term, 4 partial buffers
+//   down:    3 stages of 2 K blocks x 2 row blocks = 64 KB, 4 activation stages,
 //            4 partial buffers
 // Wide tiles (up to 128 tokens) go to moe_gemm_wide.cu.
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
   if (g.ntok == kNTokWide) return launch_gateup_wide(g, s);
-  if (g.ntok == kNTokSmall) return launch_gemm<true, kNTokSmall, 1, 6, 4, 4>(g, s);
+  if (g.ntok != kNTokSmall) return cudaErrorInvalidValue;
+  if (g.terms == 2) return launch_gemm<true, kNTokSmall, 2, 1, 6, 4, 4>(g, s);
+  if (g.terms == 1) return launch_gemm<true, kNTokSmall, 1, 1, 6, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) {
   if (g.ntok == kNTokWide) return launch_down_wide(g, s);
-  if (g.ntok == kNTokSmall) return launch_gemm<false, kNTokSmall, 2, 3, 4, 4>(g, s);
+  if (g.ntok != kNTokSmall) return cudaErrorInvalidValue;
+  if (g.terms == 3) return launch_gemm<false, kNTokSmall, 3, 2, 3, 4, 4>(g, s);
+  if (g.terms == 1) return launch_gemm<false, kNTokSmall, 1, 2, 3, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 
