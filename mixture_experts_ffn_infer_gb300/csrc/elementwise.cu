@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const uint16_t* __restrict__ shared,
                                                       const uint16_t* __restrict__ resid, int32_t n, int32_t k,
                                                       int32_t d, void* __restrict__ out, int32_t out_fp32) {
+  pdl_wait();  // launched behind the down GEMM: its rows are complete past this point
   const int nv = d / 8;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(n) * nv) return;
@@ -287,8 +288,9 @@ cudaError_t launch_combine(const uint16_t* rows_f16, const uint16_t* shared_f16,
   if (n <= 0) return cudaSuccess;
   const int64_t nv = static_cast<int64_t>(n) * (d / 8);
   const int blocks = static_cast<int>((nv + 255) / 256);
-  combine_kernel<<<blocks, 256, 0, s>>>(rows_f16, shared_f16, resid_bf16, n, k, d, out, out_fp32);
-  return cudaGetLastError();
+  // dependent launch: the CTAs are placed while the previous kernel drains and wait for it
+  return launch_maybe_overlapped(combine_kernel, blocks, 256, 0, s, true, rows_f16, shared_f16, resid_bf16, n, k, d,
+                                 out, out_fp32);
 }
 
 }  // namespace moe

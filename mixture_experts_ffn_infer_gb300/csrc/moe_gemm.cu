@@ -159,6 +159,8 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   volatile uint32_t* abort_flag = tmem_slot + 1;
   float* red = reinterpret_cast<float*>(smem + C::kRedOffset);  // [2][4 warps][NTOK] block maxima
 
+  // the down pass's dependent (the combine) may be placed now; it waits for this grid to end
+  if (!GATEUP) pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < WST; ++i) {

@@ -88,6 +88,7 @@ route_permute_kernel(const int32_t* __restrict__ ids, int32_t n, int32_t k, int3
   int32_t* warp_sums = smem + kWarps * E;  // [32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = n * k;
+  pdl_wait();  // launched behind the previous kernel in the stream: nothing is touched before it ends
 
   if (reset_err && tid == 0) *err = 0u;  // a new routing plan starts a new error record
   for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
@@ -345,9 +346,9 @@ cudaError_t launch_route_permute(const int32_t* ids, int32_t n, int32_t k, int32
     cudaError_t e = cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    route_permute_kernel<<<1, kThreads, smem, s>>>(ids, n, k, E, counts, offsets, sorted_pos, inv_pos, validate, 1,
-                                                   err, ntok, tiles, n_tiles);
-    return cudaGetLastError();
+    // dependent launch: placed while the previous kernel in the stream drains; it waits for it
+    return launch_maybe_overlapped(route_permute_kernel, 1, kThreads, smem, s, true, ids, n, k, E, counts, offsets,
+                                   sorted_pos, inv_pos, validate, 1, err, ntok, tiles, n_tiles);
   }
   if (!scratch) return cudaErrorInvalidValue;
   const int chunks = static_cast<int>((R + kChunkEntries - 1) / kChunkEntries);
