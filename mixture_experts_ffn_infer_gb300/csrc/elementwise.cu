@@ -54,7 +54,9 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
                                                                   const int32_t* __restrict__ inv_pos, int32_t n,
                                                                   int32_t k, int32_t d, uint8_t* __restrict__ xs,
                                                                   SplitLayout lay, float* __restrict__ xs_inv) {
-  // the gate/up GEMM may start streaming its weights now; it waits for these rows
+  pdl_wait();  // launched behind the routing plan, whose inv_pos it reads
+  // Everything before this kernel in the stream is complete now, so the gate/up GEMM
+  // may be placed and stream its weights (it waits for these rows, not for the weights).
   pdl_launch_dependents();
   const int64_t t = blockIdx.x;
   const int64_t R = static_cast<int64_t>(n) * k;
@@ -261,8 +263,17 @@ cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* inv_pos, i
   const int nkb = d / 128;
   const int max_groups = (nkb + kRowThreads / 32 - 1) / (kRowThreads / 32);
   const int groups = n >= sms ? 1 : max(1, min(max_groups, sms / n));
-  gather_rows_kernel<<<dim3(n, groups), kRowThreads, 0, s>>>(x_bf16, inv_pos, n, k, d, xs, lay, xs_inv);
-  return cudaGetLastError();
+  // dependent launch: placed while the routing plan finishes, waiting for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n, groups);
+  cfg.blockDim = dim3(kRowThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, x_bf16, inv_pos, n, k, d, xs, lay, xs_inv);
 }
 
 cudaError_t launch_invert_positions(const int32_t* sorted_pos, int32_t R, int32_t* inv, cudaStream_t s) {

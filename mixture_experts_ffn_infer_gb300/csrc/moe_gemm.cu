@@ -159,8 +159,11 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
   volatile uint32_t* abort_flag = tmem_slot + 1;
   float* red = reinterpret_cast<float*>(smem + C::kRedOffset);  // [2][4 warps][NTOK] block maxima
 
-  // the down pass's dependent (the combine) may be placed now; it waits for this grid to end
-  if (!GATEUP) pdl_launch_dependents();
+  // The dependent launch behind this grid (down behind gate/up, the combine behind down)
+  // may be placed now: this grid was placed only after every kernel before its own
+  // predecessor had ended, so a dependent that reads weights without waiting reads
+  // finished ones; it waits for this grid to end before it reads this grid's results.
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < WST; ++i) {
@@ -489,9 +492,11 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;
-  // gate/up after the row gather: its CTAs fit beside the gather's, so they start
-  // streaming weights at once (the gather triggers its dependents on entry)
-  return launch_maybe_overlapped(kern, g.num_sms, kThreads, C::kSmem, s, GATEUP && g.overlap, *g.w0, *g.w1,
+  // dependent launches: gate/up after the row gather (its CTAs fit beside the gather's,
+  // so they start streaming weights at once) and down after gate/up (each CTA starts
+  // streaming down weights as soon as its SM's gate/up CTA exits); both wait for
+  // their predecessor before they read activations
+  return launch_maybe_overlapped(kern, g.num_sms, kThreads, C::kSmem, s, !GATEUP || g.overlap, *g.w0, *g.w1,
                                  *g.act, a);
 }
 

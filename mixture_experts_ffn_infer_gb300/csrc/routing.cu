@@ -89,6 +89,7 @@ route_permute_kernel(const int32_t* __restrict__ ids, int32_t n, int32_t k, int3
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = n * k;
   pdl_wait();  // launched behind the previous kernel in the stream: nothing is touched before it ends
+  pdl_launch_dependents();  // the row gather may be placed now; it waits for this plan
 
   if (reset_err && tid == 0) *err = 0u;  // a new routing plan starts a new error record
   for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
