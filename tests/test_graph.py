@@ -101,3 +101,33 @@ def test_mlp_and_fp8_infer_graph_replay_matches_eager(act):
     torch.cuda.synchronize()
     assert torch.equal(out, eager) and torch.equal(out1, eager1)
     assert mx.moe_get_error(ws) == mx.MOE_OK and mx.moe_get_error(ws1) == mx.MOE_OK
+
+
+@pytest.mark.parametrize("act", [mx.MOE_ACT_EXACT, mx.MOE_ACT_FP8_DYNAMIC])
+def test_weights_written_just_before_the_call_are_the_ones_used(act):
+    # Every kernel of a call is a dependent launch of the one before, and the GEMMs stream weights
+    # without waiting; a bank overwritten in place by the kernel right before the call must still be
+    # read only after that kernel has finished (decode-sized: 16-token tiles; and wide tiles).
+    for wl in (syn.Workload("pd16", 16, 512, 256, 32, 4, seed=31), syn.Workload("pdw", 200, 512, 256, 8, 2, seed=32)):
+        c = cases.workload(wl)
+        other = cases.bank_to(syn.expert_bank(wl.num_experts, wl.d, wl.d_ff, 77), "cuda")
+        ref = mx.infer(c.x, c.ids, c.w, other, act_scheme=act)
+        tiled, tiled_other = mx.pack_bank(c.bank), mx.pack_bank(other)
+        torch.cuda.synchronize()
+        mx.infer(c.x, c.ids, c.w, tiled, act_scheme=act)            # the bank as it was
+        tiled.w_gate.copy_(tiled_other.w_gate)                       # then overwritten in place ...
+        tiled.w_down.copy_(tiled_other.w_down)
+        for nm in ("s_gate", "s_up", "s_down"):
+            getattr(tiled, nm).copy_(getattr(tiled_other, nm))
+        y = mx.infer(c.x, c.ids, c.w, tiled, act_scheme=act)         # ... and used at once
+        assert torch.equal(y, ref)
+        # the dense MLP entry point and the fused layer's path start with other kernels
+        one = syn.ExpertBank(*(t[:1].contiguous() for t in (c.bank.w_gate, c.bank.w_up, c.bank.w_down,
+                                                            c.bank.s_gate, c.bank.s_up, c.bank.s_down)))
+        one_other = syn.ExpertBank(*(t[:1].contiguous() for t in (other.w_gate, other.w_up, other.w_down,
+                                                                  other.s_gate, other.s_up, other.s_down)))
+        ref1 = mx.mlp_forward(c.x, one_other, act_scheme=act)
+        mx.mlp_forward(c.x, one, act_scheme=act)
+        for nm in ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down"):
+            getattr(one, nm).copy_(getattr(one_other, nm))
+        assert torch.equal(mx.mlp_forward(c.x, one, act_scheme=act), ref1)
