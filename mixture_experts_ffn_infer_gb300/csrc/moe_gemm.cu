@@ -27,10 +27,11 @@
 //               into its own ring, so neither ring throttles the other.
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=TT NTOK, K=32) per
 //               weight block into a fresh fp32 partial in tensor memory.
-//   warps 4-7   epilogue: per token, sum the three term columns, multiply by
-//               the weight block's fp32 scale and the activation block's 2^-s
-//               and add to fp32 accumulators in registers - the exact
-//               block-scaled product of the dequantised operands.
+//   warps 4-7   epilogue: per token, sum its TT term columns, multiply by
+//               the weight block's fp32 scale and the activation block's factor
+//               (2^-s, or the FP8 scale) and add to fp32 accumulators in
+//               registers - the exact block-scaled product of the dequantised
+//               operands.
 //
 // After the last K block the epilogue writes, per valid token column,
 //   gate/up pass : h = silu(g) * u in the split format (one block scale per
@@ -39,9 +40,11 @@
 //                  other two terms zero
 //   down pass    : f16(topk_weight * o) -> rows[flat position][feature], both blocks
 //
-// Every wait is bounded; a wait that gives up raises the CTA's abort flag and
-// the device error word, the roles drain their in-flight copies and MMAs and
-// the kernel returns normally.
+// Both passes are dependent launches (gate/up behind the row gather, down
+// behind gate/up): the weight producer starts at once, the activation producer
+// and the epilogue wait for the previous grid first.  Every wait is bounded; a
+// wait that gives up raises the CTA's abort flag and the device error word, the
+// roles drain their in-flight copies and MMAs and the kernel returns normally.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 

@@ -29,8 +29,8 @@
 // Warps (384 threads = 3 warpgroups, one CTA per SM, persistent over the unit
 // list; warpgroup 0 hands registers to the epilogue warpgroups):
 //   0      weight producer: the K block's two 16 KB tiles (one 32 KB bulk copy
-//          of the tiled layout, or 3-D TMA of the row-major layout), L2
-//          prefetch ahead
+//          of the tiled layout, or 3-D TMA of the row-major layout), and an L2
+//          prefetch ahead when several token tiles share an expert's weights
 //   1      MMA issuer (one thread)
 //   2      activation producer: one 3-D TMA box [terms][128 rows][128 bytes]
 //          per K block
@@ -40,12 +40,13 @@
 //
 // At the end of a unit the gate/up epilogue forms h = silu(g) * u and writes
 // it as three term planes, one exponent per (token, 128 features) from the
-// maximum over both feature halves (their float exponents, exchanged as bytes); the down epilogue writes
-// f16(topk_weight * o) to the row's flat position.  With dynamic FP8
-// activations (TX = 1: one term per value) the gate/up epilogue exchanges the
-// halves' maxima as floats and writes one plane of codes of h / s, s = amax / 448.  Every wait is bounded; a
-// wait that gives up raises the abort flag and the device error word, and
-// every role drains what it has in flight before the kernel returns.
+// maximum over both feature halves (their float exponents, exchanged as
+// bytes); the down epilogue writes f16(topk_weight * o) to the row's flat
+// position.  With dynamic FP8 activations (TX = 1: one term per value) the
+// gate/up epilogue exchanges the halves' maxima as floats and writes one plane
+// of codes of h / s, s = amax / 448.  Every wait is bounded; a wait that gives
+// up raises the abort flag and the device error word, and every role drains
+// what it has in flight before the kernel returns.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
