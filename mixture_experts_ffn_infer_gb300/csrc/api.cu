@@ -325,16 +325,18 @@ moe_status experts_pass(const moe_dims* d, int64_t n, const void* x, const float
   int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
   const bool fp8 = fp8_act(d);
   const int x_terms = x_terms_of(fp8);
+  // The tile list is complete before the gather runs: the GEMMs are dependent launches
+  // whose weight producer and MMA issuer read it without waiting.
+  if (!plan_ready) {
+    MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
+    tr.after("build_tiles");
+  }
   if (gather) {
     int32_t* ip = at<int32_t>(ws, L.inv_pos);
     if (!plan_ready) MOE_CHECK_CUDA(launch_invert_positions(sorted_pos, R, ip, s));
     MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), ip, static_cast<int32_t>(n), d->top_k, d->d,
                                       xs, rows_layout(R, d->num_experts, d->d, x_terms, fp8), xs_inv, s));
     tr.after("gather_rows");
-  }
-  if (!plan_ready) {
-    MOE_CHECK_CUDA(launch_build_tiles(offsets, d->num_experts, tile_tokens(R, d->num_experts), tiles, n_tiles, s));
-    tr.after("build_tiles");
   }
   return run_gemms(gather, fp8, w, d->d, d->d_ff, d->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
                    at<float>(ws, L.h_inv), tiles, n_tiles, sorted_pos, topk_weight, rows, at<uint32_t>(ws, L.err), s,
