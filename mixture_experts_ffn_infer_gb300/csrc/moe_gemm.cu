@@ -513,8 +513,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 // of gate/up's bf16 features, 48 for h's three in down, 16 under dynamic FP8):
 //   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 activation stages of
 //            2 KB per term, 4 partial buffers
-//   down:    3 stages of 2 K blocks x 2 row blocks = 64 KB, 4 activation stages,
-//            4 partial buffers
+//   down:    5 stages of 1 K block x 2 row blocks = 32 KB, 4 activation stages,
+//            4 partial buffers (five 32 KB stages measured 2.7 % faster than
+//            three of 64 KB)
 // Wide tiles (up to 128 tokens) go to moe_gemm_wide.cu.
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
   if (g.ntok == kNTokWide) return launch_gateup_wide(g, s);
@@ -526,8 +527,8 @@ cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) {
   if (g.ntok == kNTokWide) return launch_down_wide(g, s);
   if (g.ntok != kNTokSmall) return cudaErrorInvalidValue;
-  if (g.terms == 3) return launch_gemm<false, kNTokSmall, 3, 2, 3, 4, 4>(g, s);
-  if (g.terms == 1) return launch_gemm<false, kNTokSmall, 1, 2, 3, 4, 4>(g, s);
+  if (g.terms == 3) return launch_gemm<false, kNTokSmall, 3, 1, 5, 4, 4>(g, s);
+  if (g.terms == 1) return launch_gemm<false, kNTokSmall, 1, 1, 5, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 
