@@ -24,7 +24,8 @@ constexpr int kMaxTopK = 32;
 // per term for wide tiles; SplitLayout) plus one fp32 exponent factor per
 // (128 columns, row).
 struct Layout {
-  size_t err = 0, n_tiles = 64, route = 256, route_end = 256, tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
+  size_t err = 0, n_tiles = 64, route = 256, route_end = 256;
+  size_t tiles = 0, tiles_sh = 0, counts = 0, offsets = 0, sorted_pos = 0, inv_pos = 0;
   size_t xs = 0, xs_inv = 0, h = 0, h_inv = 0, xs_sh = 0, xs_sh_inv = 0, h_sh = 0, h_sh_inv = 0, sh_out = 0;
   size_t rows = 0, total = 0;
 };
@@ -221,8 +222,9 @@ struct Tracer {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
-// Activation map of one GEMM pass: the 2-D map of 16-token tiles, or the planar
-// map of wide tiles (box of 128 rows x all terms).
+// Activation map of one GEMM pass: the 3-D map of 16-token tiles (rows
+// interleaved with their term slots, box of 16 rows x the live terms), or the
+// planar map of wide tiles (box of 128 rows x all terms).
 struct ActMaps {
   CUtensorMap m16;
   CUtensorMap box;

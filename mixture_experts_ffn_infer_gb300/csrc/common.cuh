@@ -51,9 +51,10 @@ struct TileDesc {
 };
 
 // Token tile widths of the grouped GEMMs.  Decode-like batches (a few rows per
-// expert) use 16-token tiles whose three activation terms sit side by side on
-// the MMA's N axis (N = 48); from 24 rows per expert on, tiles of up to 128
-// tokens on the MMA's M side with the terms stacked along K.
+// expert) use 16-token tiles whose live activation terms sit side by side on
+// the MMA's N axis (N = 16 x terms: 32 for x, 48 for h, 16 under dynamic FP8);
+// from 24 rows per expert on, tiles of up to 128 tokens on the MMA's M side
+// with the terms stacked along K.
 constexpr int kNTokSmall = 16;
 constexpr int kNTokWide = 128;
 __host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
@@ -76,7 +77,8 @@ struct SplitLayout {
   int32_t fp8;
 };
 inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms, bool fp8) {
-  return wide ? SplitLayout{K, rows * K, fp8 ? 1 : terms, fp8 ? 1 : 0} : SplitLayout{3 * K, K, fp8 ? 1 : terms, fp8 ? 1 : 0};
+  const int32_t t = fp8 ? 1 : terms, f = fp8 ? 1 : 0;
+  return wide ? SplitLayout{K, rows * K, t, f} : SplitLayout{3 * K, K, t, f};
 }
 
 // Launch with programmatic stream serialization when `overlap`: the kernel may
