@@ -505,10 +505,12 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 
 }  // namespace
 
-// Weight stages are large on purpose: on GB300 a CTA's stream of bulk copies
-// completes at a roughly fixed number of copy groups per memory round trip, so
-// the bytes per stage set the bandwidth (a probe streaming into shared memory
-// reached 7.0 TB/s with 64 KB stages and 2.0 TB/s with 16 KB stages).
+// Each weight stage is one bulk copy of 32 KB: on GB300 an SM completes bulk
+// copies at a roughly fixed rate (about 3.5 million per second) up to 32 KB, so
+// the bytes per copy and the copies in flight set the bandwidth (a probe
+// streaming from HBM into shared memory: 8 KB copies cap at 29 GB/s per SM;
+// 32 KB copies reach 47-48 GB/s per SM, 7.4 TB/s in total, with two or more
+// in flight).
 // Decode-sized tiles (16 tokens; MMA N = 16 per live term: 32 for the two terms
 // of gate/up's bf16 features, 48 for h's three in down, 16 under dynamic FP8):
 //   gate/up: 6 stages of 1 K block x (gate, up) = 32 KB, 4 activation stages of
