@@ -11,7 +11,8 @@
 // One persistent CTA per SM walks a list of work units.  A unit is one tile of
 // at most NTOK sorted rows of one expert times two blocks of 128 weight rows:
 // gate and up of the same 128 output features (gate/up pass), or down row
-// blocks 2j and 2j + 1 (down pass).  The weights are the MMA's M side (128
+// blocks 2j and 2j + 1 (down pass; the units of a last round that would leave
+// most SMs idle are cut into single row blocks).  The weights are the MMA's M side (128
 // rows) and the tokens its N side ("swap AB").  The e4m3 weight tiles go from
 // global memory to shared memory by bulk copy (tiled layout: both blocks of
 // KPS consecutive K blocks in one copy) or TMA (row-major layout) and
@@ -107,18 +108,48 @@ struct GemmArgs {
   uint32_t* err;
 };
 
+// The unit list.  Units [0, n_pair) are token tile u / upt times its unit row
+// u % upt (two weight blocks).  Down pass: when the last, partial round of units
+// would keep at most half of the CTAs busy, its units are cut into their two
+// row blocks (units n_pair + 2i and n_pair + 2i + 1 are the blocks of unit
+// n_pair + i), so twice as many SMs stream the tail, each half as long.  Only
+// with an even number of row blocks, where every pair is complete.
+struct UnitList {
+  int n_pair;
+  int total;
+};
+
+__device__ __forceinline__ UnitList unit_list(const GemmArgs& a, int upt) {
+  const int U = *a.n_tiles * upt, G = static_cast<int>(gridDim.x);
+  const int q = U / G, r = U - q * G;
+  if (!a.pair || (a.n_nb & 1) || r == 0 || 2 * r > G) return UnitList{U, U};
+  return UnitList{q * G, q * G + 2 * r};
+}
+
 struct Unit16 {
-  int e, ru, nb0, nb1;
+  int tile, ru, nb0, nb1;
+  int half;  // -1: both blocks of the unit row; 0 or 1: that block of the down pair alone
   bool has1;
 };
 
-__device__ __forceinline__ Unit16 unit16(const GemmArgs& a, const TileDesc& td, int u, int upt) {
+__device__ __forceinline__ Unit16 unit16(const GemmArgs& a, int u, int upt, const UnitList& L) {
   Unit16 x;
-  x.e = td.expert;
-  x.ru = u % upt;
-  x.nb0 = a.pair ? 2 * x.ru : x.ru;
-  x.nb1 = a.pair ? 2 * x.ru + 1 : x.ru;
-  x.has1 = x.nb1 < a.n_nb;
+  int v = u;
+  x.half = -1;
+  if (u >= L.n_pair) {
+    v = L.n_pair + ((u - L.n_pair) >> 1);
+    x.half = (u - L.n_pair) & 1;
+  }
+  x.tile = v / upt;
+  x.ru = v % upt;
+  if (x.half >= 0) {
+    x.nb0 = x.nb1 = 2 * x.ru + x.half;
+    x.has1 = false;
+  } else {
+    x.nb0 = a.pair ? 2 * x.ru : x.ru;
+    x.nb1 = a.pair ? 2 * x.ru + 1 : x.ru;
+    x.has1 = x.nb1 < a.n_nb;
+  }
   return x;
 }
 
@@ -205,7 +236,8 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
 
   const int n_nb = a.n_nb, num_kb = a.num_kb;
   const int upt = a.pair ? (n_nb + 1) / 2 : n_nb;  // units per tile
-  const int total_units = *a.n_tiles * upt;
+  const UnitList L = unit_list(a, upt);
+  const int total_units = L.total;
   // tiled layout: K block kb of unit row ru of expert e, both blocks (32 KB)
   auto unit_off = [&](int e, int ru, int kb) {
     return ((static_cast<int64_t>(e) * upt + ru) * num_kb + kb) * C::kWKb;
@@ -220,7 +252,8 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       uint32_t w_issued = 0;  // weight stages issued
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit16 un = unit16(a, a.tiles[u / upt], u, upt);
+        const Unit16 un = unit16(a, u, upt, L);
+        const int e = a.tiles[un.tile].expert;
         for (int kb = 0; kb < num_kb; kb += KPS) {
           const uint32_t it = w_issued;
           const int sw = it % WST;
@@ -230,17 +263,23 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             break;
           }
           const uint32_t wst = sbase + sw * C::kWStage;
-          if (a.w_tiled) {
+          if (a.w_tiled && un.half < 0) {
             // the stage's K blocks, both weight blocks each, are one contiguous
             // region already in the swizzled image: one bulk copy
             mbar_arrive_expect_tx(full_w(sw), nk * C::kWKb);
-            bulk_load(wst, a.w_tiled + unit_off(un.e, un.ru, kb), nk * C::kWKb, full_w(sw), pol_w);
+            bulk_load(wst, a.w_tiled + unit_off(e, un.ru, kb), nk * C::kWKb, full_w(sw), pol_w);
+          } else if (a.w_tiled) {
+            // one block of the pair: its 16 KB tile of each K block, to the stage's first slot
+            mbar_arrive_expect_tx(full_w(sw), nk * C::kWTile);
+            for (int j = 0; j < nk; ++j)
+              bulk_load(wst + j * C::kWKb, a.w_tiled + unit_off(e, un.ru, kb + j) + un.half * C::kWTile, C::kWTile,
+                        full_w(sw), pol_w);
           } else {
             mbar_arrive_expect_tx(full_w(sw), nk * (un.has1 ? 2 : 1) * C::kWTile);
             for (int j = 0; j < nk; ++j) {
-              tma_load_3d(wst + j * C::kWKb, &tm_w0, full_w(sw), (kb + j) * 128, un.nb0 * 128, un.e, pol_w);
+              tma_load_3d(wst + j * C::kWKb, &tm_w0, full_w(sw), (kb + j) * 128, un.nb0 * 128, e, pol_w);
               if (un.has1)
-                tma_load_3d(wst + j * C::kWKb + C::kWTile, &tm_w1, full_w(sw), (kb + j) * 128, un.nb1 * 128, un.e,
+                tma_load_3d(wst + j * C::kWKb + C::kWTile, &tm_w1, full_w(sw), (kb + j) * 128, un.nb1 * 128, e,
                             pol_w);
             }
           }
@@ -259,7 +298,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       uint32_t b_issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int row0 = a.tiles[u / upt].row_start;
+        const int row0 = a.tiles[unit16(a, u, upt, L).tile].row_start;
         for (int kb = 0; kb < num_kb; ++kb) {
           const uint32_t it = b_issued;
           const int sb = it % BST;
@@ -284,7 +323,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
       uint32_t it = 0, wt = 0;  // K blocks and weight stages consumed
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const bool has1 = a.pair ? (2 * (u % upt) + 1 < n_nb) : true;
+        const bool has1 = unit16(a, u, upt, L).has1;
         for (int kb0 = 0; ok && kb0 < num_kb; kb0 += KPS, ++wt) {
           const int sw = wt % WST;
           const int nk = min(KPS, num_kb - kb0);
@@ -331,10 +370,10 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     uint32_t it = 0, ui = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
-      const TileDesc td = a.tiles[u / upt];
-      const Unit16 un = unit16(a, td, u, upt);
-      const float* sc0 = a.s0 + (static_cast<int64_t>(un.e) * n_nb + un.nb0) * num_kb;
-      const float* sc1 = a.s1 + (static_cast<int64_t>(un.e) * n_nb + (un.has1 ? un.nb1 : un.nb0)) * num_kb;
+      const Unit16 un = unit16(a, u, upt, L);
+      const TileDesc td = a.tiles[un.tile];
+      const float* sc0 = a.s0 + (static_cast<int64_t>(td.expert) * n_nb + un.nb0) * num_kb;
+      const float* sc1 = a.s1 + (static_cast<int64_t>(td.expert) * n_nb + (un.has1 ? un.nb1 : un.nb0)) * num_kb;
       float acc[2][NTOK];
 #pragma unroll
       for (int m = 0; m < 2; ++m)

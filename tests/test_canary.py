@@ -3,7 +3,8 @@ inside a larger allocation whose surrounding bytes hold a fixed pattern, and the
 pattern must be intact after the call.  Covers the workspace and the outputs of
 moe_permute, moe_experts_forward, moe_combine, moe_infer, moe_layer_forward and
 moe_mlp_forward, on both tile widths and both activation schemes, including a
-ragged batch whose last tile is partial."""
+ragged batch whose last tile is partial and a 16-token batch whose down units
+are single row blocks."""
 
 import pytest
 import torch
@@ -46,6 +47,7 @@ def _ws(dm, n, dff_sh=0):
 
 
 @pytest.mark.parametrize("wl", [syn.Workload("c16", 37, 384, 256, 5, 3, seed=41),     # 16-token tiles, ragged
+                                syn.Workload("c16s", 37, 512, 256, 5, 3, seed=44),    # down units cut into single blocks
                                 syn.Workload("cw", 300, 256, 384, 3, 2, seed=42)])    # wide tiles, partial last tile
 @pytest.mark.parametrize("act", [mx.MOE_ACT_EXACT, mx.MOE_ACT_FP8_DYNAMIC])
 def test_routed_calls_write_only_their_buffers(wl, act):

@@ -48,6 +48,7 @@ def test_tiny_infer_bf16_and_fp32_outputs():
     (40, 256, 128, 64, 32, 12),    # the largest top-k (32): 1280 rows over 64 experts
     (24, 128, 256, 1024, 4, 13),   # the largest expert count (1024), almost every expert empty
     (200, 256, 128, 40, 32, 14),   # top-k 32 with 160 rows per expert: wide tiles
+    (64, 1024, 256, 40, 8, 22),    # 176 down units on 152 SMs: 152 pairs, then 48 single row blocks
 ])
 def test_small_shapes_infer(n, d, dff, E, k, seed):
     wl = syn.Workload("s", n, d, dff, E, k, seed=seed)

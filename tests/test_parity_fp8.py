@@ -66,6 +66,7 @@ def test_tiny_fp8_matches_oracle_and_scheme_accuracy():
     (600, 256, 256, 2, 1, 6),      # tiles of 128, 128 and 44 rows
     (150, 1152, 256, 4, 2, 8),     # nine row blocks of down: the last pair has one block
     (40, 256, 128, 64, 32, 12),    # top-k 32 over 64 experts
+    (64, 1024, 256, 40, 8, 22),    # 176 down units on 152 SMs: 152 pairs, then 48 single row blocks
 ])
 def test_small_shapes_fp8(n, d, dff, E, k, seed):
     wl = syn.Workload("s", n, d, dff, E, k, seed=seed)
