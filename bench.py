@@ -134,11 +134,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _traffic(workload, kernel):
-    """DRAM bytes per launch from the committed ncu summary, or None when the kernel's
-    source file has changed since those counters were taken."""
+def _traffic(workload, kernel, fp8=False):
+    """DRAM bytes per launch from the committed ncu summary of this workload and activation scheme,
+    or None when there is none or the kernel's source file has changed since its counters were taken."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    prof = os.path.join(ROOT, "profiles", f"traffic_{workload}{'_fp8' if fp8 else ''}.json")
     try:
         rec = json.load(open(prof))
         src = os.path.join(ROOT, "mixture_experts_ffn_infer_gb300", "csrc", rec["source"])
@@ -367,8 +367,7 @@ def run_ours(args, rank, world, local_rank):
     tensor_src = (f"{bf16_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (nominal e4m3 / bf16 dense ratio)")
     hbm_label = hbm_src + " (MEASURED_PEAKS.json hbm_gbs)" if hbm_src == "measured" else hbm_src
     tflops = alg["step_flops"] / (ms_step / 1e3) / 1e12
-    # the recorded counters are of the exact scheme's kernels
-    traffic = _traffic(args.workload, dominant) if not fp8 else None
+    traffic = _traffic(args.workload, dominant, fp8)
     result = {
         "metric": METRIC,
         "value": value,
@@ -395,7 +394,7 @@ def run_ours(args, rank, world, local_rank):
                                     hbm, hbm_label, e4m3_peak, tensor_src, traffic),
         "down_roofline": kernel_roofline("down_scatter", alg["down_bytes"], alg["down_flops"],
                                          kern_ms.get("down_scatter"), hbm, hbm_label, e4m3_peak, tensor_src,
-                                         _traffic(args.workload, "down_scatter") if not fp8 else None),
+                                         _traffic(args.workload, "down_scatter", fp8)),
         "step_roofline": {"bytes": alg["step_bytes"], "flops": alg["step_flops"], "t_roof_ms_hbm": step_roof_ms,
                           "frac_hbm": step_roof_ms / ms_step, "tflops": tflops,
                           "frac_bf16_sustained": tflops / bf16, "bf16_peak_source": bf16_src},

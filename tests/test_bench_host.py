@@ -57,3 +57,25 @@ def test_missing_kernel_time_reports_no_fraction():
     _, a = _alg("k2_decode", 104)
     r = bench.kernel_roofline("down_scatter", a["down_bytes"], a["down_flops"], None, HBM, "m", E4M3, "m", None)
     assert r["achieved"] is None and r["frac"] is None and r["bound"] == "hbm"
+
+
+def test_traffic_record_is_used_only_for_its_scheme_and_unchanged_source(tmp_path, monkeypatch):
+    import hashlib
+    import json
+    src = tmp_path / "mixture_experts_ffn_infer_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    sha = hashlib.sha256(b"kernel v1\n").hexdigest()
+    (tmp_path / "profiles" / "traffic_w.json").write_text(json.dumps(
+        {"source": "k.cu", "source_sha256": sha, "gateup_swiglu": 111}))
+    (tmp_path / "profiles" / "traffic_w_fp8.json").write_text(json.dumps(
+        {"source": "k.cu", "source_sha256": sha, "gateup_swiglu": 222}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._traffic("w", "gateup_swiglu") == 111
+    assert bench._traffic("w", "gateup_swiglu", fp8=True) == 222
+    assert bench._traffic("w", "down_scatter") is None          # no counters for that kernel
+    assert bench._traffic("other", "gateup_swiglu") is None     # no record for the workload
+    (src / "k.cu").write_text("kernel v2\n")                    # the kernel changed since the capture
+    assert bench._traffic("w", "gateup_swiglu") is None
+    assert bench._traffic("w", "gateup_swiglu", fp8=True) is None
