@@ -43,12 +43,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 
 // One GEMM tile of the grouped GEMMs: `n_valid` consecutive rows of the
 // sorted activation matrix starting at `row_start`, all routed to `expert`.
+// The tiles of one expert's slice are grouped into chunks of at most
+// kTileChunk consecutive tiles; `chunk` holds the tile's index within its chunk
+// (bits 0-7) and the chunk's tile count (bits 8-15).
 struct TileDesc {
   int32_t expert;
   int32_t row_start;
   int32_t n_valid;
-  int32_t pad;
+  int32_t chunk;
 };
+
+constexpr int kTileChunk = 8;
+__host__ __device__ inline int32_t tile_chunk_code(int idx_in_slice, int tiles_in_slice) {
+  const int c = idx_in_slice / kTileChunk;
+  const int left = tiles_in_slice - c * kTileChunk;
+  return (idx_in_slice % kTileChunk) | ((left < kTileChunk ? left : kTileChunk) << 8);
+}
 
 // Token tile widths of the grouped GEMMs.  Decode-like batches (a few rows per
 // expert) use 16-token tiles whose live activation terms sit side by side on

@@ -106,9 +106,17 @@ struct Unit {
   bool has1;
 };
 
+// Unit u.  Within each chunk of an expert's tiles the units run weight-row
+// block first: the chunk's n tiles take units first*upt .. (first+n)*upt - 1,
+// unit row j of tile first + i being unit first*upt + j*n + i, so the tiles
+// that read the same weights are neighbours in the unit list and run at the
+// same time (their weights are read from DRAM once and from L2 after that).
 __device__ __forceinline__ Unit unit_of(const WideArgs& a, int u, int upt) {
-  const TileDesc td = a.tiles[u / upt];
-  const int j = u % upt;
+  const int code = a.tiles[u / upt].chunk;  // a tile of the same chunk
+  const int first = u / upt - (code & 0xff), n = code >> 8;
+  const int l = u - first * upt;
+  const TileDesc td = a.tiles[first + l % n];
+  const int j = l / n;
   Unit x;
   x.e = td.expert;
   x.row0 = td.row_start;
@@ -299,7 +307,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       uint32_t ai = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int row0 = a.tiles[u / upt].row_start;
+        const int row0 = unit_of(a, u, upt).row0;
         for (int kb = 0; kb < num_kb; ++kb) {
           const int sa = ai % AST;
           if (!wait_bounded(empty_a(sa), ((ai / AST) & 1) ^ 1, abort_flag, a.err)) {

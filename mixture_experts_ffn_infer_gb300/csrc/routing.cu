@@ -73,7 +73,11 @@ __device__ void cta_build_tiles(const int32_t* __restrict__ offsets, int E, int 
   int t = block_exclusive_scan(local, warp_sums, &total);
   for (int e = e0; e < e1; ++e) {
     const int beg = offsets[e], end = offsets[e + 1];
-    for (int r = beg; r < end; r += ntok) tiles[t++] = TileDesc{e, r, min(ntok, end - r), 0};
+    const int nt_e = (end - beg + ntok - 1) / ntok;
+    for (int i = 0; i < nt_e; ++i) {
+      const int r = beg + i * ntok;
+      tiles[t++] = TileDesc{e, r, min(ntok, end - r), tile_chunk_code(i, nt_e)};
+    }
   }
   if (tid == 0) *n_tiles = total;
 }
@@ -309,7 +313,7 @@ build_tiles_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t ntok,
 __global__ void identity_tiles_kernel(int32_t rows, int32_t ntok, TileDesc* tiles, int32_t* n_tiles) {
   const int nt = (rows + ntok - 1) / ntok;
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nt; t += gridDim.x * blockDim.x)
-    tiles[t] = TileDesc{0, t * ntok, min(ntok, rows - t * ntok), 0};
+    tiles[t] = TileDesc{0, t * ntok, min(ntok, rows - t * ntok), tile_chunk_code(t, nt)};
   if (blockIdx.x == 0 && threadIdx.x == 0) *n_tiles = nt;
 }
 
