@@ -63,6 +63,10 @@ def _bf16_peak(sustained):
 # dense e4m3 / bf16 tensor throughput of the part (4.5 / 2.25 PFLOP/s nominal)
 FP8_PER_BF16 = 2.0
 
+# what the tensor cores compute in, per activation scheme
+DTYPE_EXACT = "e4m3 weights x e4m3 split-term activations (exact scheme), fp32 accumulation"
+DTYPE_FP8 = "e4m3 weights x e4m3 dynamic activations (amax/448 per 128), fp32 accumulation"
+
 
 def kernel_roofline(kernel, alg_bytes, alg_flops, ms, hbm_gbs, hbm_src, e4m3_tflops, tensor_src, traffic):
     """A kernel's algorithmic work against the roof that bounds it: HBM when its bytes take longer at the
@@ -201,7 +205,6 @@ def job_tokens_per_s(tokens_per_rank, world, steps, ms_total_max):
 
 def run_ours(args, rank, world, local_rank):
     import torch
-    import torch.distributed as dist
 
     import mixture_experts_ffn_infer_gb300 as mx
     from mixture_experts_ffn_infer_gb300 import synthetic as syn
@@ -214,10 +217,34 @@ def run_ours(args, rank, world, local_rank):
     if args.n_tokens:
         wl = syn.Workload(**{**wl.__dict__, "n_tokens": args.n_tokens})
     mx.load_library()
+    # all 384 experts' weights resident in HBM, prepared once at load time into the tiled streaming layout;
+    # the row-major bank stays for the CPU baseline, which reads the model's layout
+    bank = syn.expert_bank(wl.num_experts, wl.d, wl.d_ff, syn.bank_seed_of(wl), dev)
+    bank_t = mx.pack_bank(bank)
+    torch.cuda.synchronize(dev)
+    result = measure(args, wl, args.workload, bank, bank_t, rank, world, local_rank, dev)
+    # the default run also measures the prefill batch on the same resident bank: the metric names both
+    # the decode (HBM) and the prefill roofline
+    pre = syn.WORKLOADS["k2_prefill"]
+    if (args.workload == "k2_decode" and not args.no_prefill and not args.num_experts and not args.n_tokens
+            and syn.bank_seed_of(pre) == syn.bank_seed_of(wl)):
+        result["prefill"] = measure(args, pre, "k2_prefill", bank, bank_t, rank, world, local_rank, dev)
+    return result
+
+
+def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
+    """One workload: W warm-up steps, K untimed-event steps timed as a whole (the headline), then a
+    separate sample of steps with events around the GEMMs (per-kernel times), the host-buffer end-to-end
+    leg and the CPU oracle baseline."""
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_ffn_infer_gb300 as mx
+    from mixture_experts_ffn_infer_gb300 import synthetic as syn
+
     # each rank its own batch (seed offset by rank), the same resident weights
     rank_wl = rank_workload(wl, rank)
     x, ids, w, gain = syn.make_host_inputs(rank_wl)
-    bank = syn.expert_bank(wl.num_experts, wl.d, wl.d_ff, syn.bank_seed_of(wl), dev)
     shared = syn.expert_bank(1, wl.d, wl.d_ff_shared, wl.seed + 1_000_003, dev) if wl.full_block else None
     n = x.shape[0]
     xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
@@ -227,33 +254,11 @@ def run_ours(args, rank, world, local_rank):
     dff_sh = wl.d_ff_shared if wl.full_block else 0
     ws = mx.workspace(dm, n, dff_sh, dev)
     out = torch.empty(n, wl.d, dtype=torch.bfloat16, device=dev)
-    # weights are prepared once at load time into the tiled streaming layout; the
-    # row-major bank stays for the CPU baseline, which reads the model's layout
-    bank_t = mx.pack_bank(bank)
     shared_t = mx.pack_bank(shared) if shared is not None else None
     torch.cuda.synchronize(dev)
     W = mx.weights(bank_t)
     WS = mx.weights(shared_t) if shared_t is not None else None
     stream = torch.cuda.current_stream(dev)
-
-    # Per-kernel events on a sample of about 30 of the timed steps, spread evenly: an event
-    # between two kernels costs the stream about a launch gap and blocks the gate/up GEMM's
-    # early start behind the gather, so the other steps run as a caller runs them.  Every
-    # step's trace still counts the kernels it launched.
-    n_ev = 12
-    trace_every = max(1, args.steps // 30)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] if k % trace_every == 0 else []
-           for k in range(args.steps)]
-    traces = []
-    for k in range(args.steps):
-        t = mx.moe_trace()
-        for i, e in enumerate(evs[k]):
-            e.record(stream)  # materialise the event handle
-            t.events[i] = e.cuda_event
-        t.n_events = len(evs[k])
-        t.gemms_only = 1   # events only around the GEMMs
-        traces.append(t)
-    torch.cuda.synchronize(dev)
 
     def step(trace=None, xin=xd, idin=idsd, win=wd, o=out):
         if wl.full_block:
@@ -269,6 +274,11 @@ def run_ours(args, rank, world, local_rank):
     if st != mx.MOE_OK:
         raise RuntimeError(f"device error after warm-up: {mx.STATUS.get(st)}")
 
+    # The headline: K steps as a caller runs them, no events between kernels.  A trace without events
+    # only counts the kernels each call launched.
+    counters = [mx.moe_trace() for _ in range(args.steps)]
+    for t in counters:
+        t.n_events = 0
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -279,24 +289,39 @@ def run_ours(args, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for k in range(args.steps):
-        step(traces[k])
+        step(counters[k])
     t1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    launches = sum(t.n_launched for t in counters)
 
-    # per-kernel durations from the trace events of the sampled timed steps
+    # Per-kernel durations: a separate sample of steps, each with events on the launching stream just before
+    # the first grouped GEMM and after each (an event between two kernels costs the stream about a launch
+    # gap, so these steps stay out of the headline).
+    n_traced = min(args.steps, 30)
+    n_ev = 12
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_traced)]
+    traces = []
+    for k in range(n_traced):
+        t = mx.moe_trace()
+        for i, e in enumerate(evs[k]):
+            e.record(stream)  # materialise the event handle
+            t.events[i] = e.cuda_event
+        t.n_events = n_ev
+        t.gemms_only = 1
+        traces.append(t)
+    torch.cuda.synchronize(dev)
+    for k in range(n_traced):
+        step(traces[k])
+    torch.cuda.synchronize(dev)
     per_kernel = {}
-    launches = 0
-    for k in range(args.steps):
+    for k in range(n_traced):
         t = traces[k]
-        nrec = t.n_recorded
-        launches += t.n_launched
-        for i in range(nrec - 1):
-            lab = t.labels[i].decode()
-            per_kernel.setdefault(lab, []).append(evs[k][i].elapsed_time(evs[k][i + 1]))
+        for i in range(t.n_recorded - 1):
+            per_kernel.setdefault(t.labels[i].decode(), []).append(evs[k][i].elapsed_time(evs[k][i + 1]))
     kern_ms = {k: statistics.mean(v) for k, v in per_kernel.items()}
 
     # end to end through the same C ABI with host buffers: every step copies its inputs from pinned
@@ -347,9 +372,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_run(args.steps)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1)
-    if not args.no_e2e:
-        e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     st = mx.moe_get_error(ws, stream)
     if st != mx.MOE_OK:
         raise RuntimeError(f"device error in the timed region: {mx.STATUS.get(st)}")
@@ -367,7 +390,7 @@ def run_ours(args, rank, world, local_rank):
     tensor_src = (f"{bf16_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (nominal e4m3 / bf16 dense ratio)")
     hbm_label = hbm_src + " (MEASURED_PEAKS.json hbm_gbs)" if hbm_src == "measured" else hbm_src
     tflops = alg["step_flops"] / (ms_step / 1e3) / 1e12
-    traffic = _traffic(args.workload, dominant, fp8)
+    traffic = _traffic(wl_name, dominant, fp8)
     result = {
         "metric": METRIC,
         "value": value,
@@ -379,10 +402,9 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        # the tensor cores multiply e4m3 weights by e4m3 activation terms and accumulate in fp32
-        "dtype": "e4m3",
+        "dtype": DTYPE_FP8 if fp8 else DTYPE_EXACT,
         "data": "synthetic",
-        "config": {"workload": args.workload, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
+        "config": {"workload": wl_name, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
                    "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
                    "full_block": wl.full_block, "weights": "e4m3, fp32 scale per 128x128 block, tiled layout",
                    "act_scheme": "fp8_dynamic" if fp8 else "exact",
@@ -394,12 +416,13 @@ def run_ours(args, rank, world, local_rank):
                                     hbm, hbm_label, e4m3_peak, tensor_src, traffic),
         "down_roofline": kernel_roofline("down_scatter", alg["down_bytes"], alg["down_flops"],
                                          kern_ms.get("down_scatter"), hbm, hbm_label, e4m3_peak, tensor_src,
-                                         _traffic(args.workload, "down_scatter", fp8)),
+                                         _traffic(wl_name, "down_scatter", fp8)),
         "step_roofline": {"bytes": alg["step_bytes"], "flops": alg["step_flops"], "t_roof_ms_hbm": step_roof_ms,
                           "frac_hbm": step_roof_ms / ms_step, "tflops": tflops,
-                          "frac_bf16_sustained": tflops / bf16, "bf16_peak_source": bf16_src},
+                          "frac_bf16_sustained": tflops / bf16,
+                          "frac_e4m3_sustained": tflops / e4m3_peak, "bf16_peak_source": bf16_src},
         "kernel_ms": kern_ms,
-        "kernel_ms_steps": len(range(0, args.steps, trace_every)),   # timed steps that carried the events
+        "kernel_ms_steps": n_traced,   # separate steps with events around the GEMMs, after the timed region
         "e2e": None if args.no_e2e else {"value": tokens * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * 2 + ids.numel() * 4 + w.numel() * 4),
                 "d2h_bytes_per_step": int(n * wl.d * 2), "ms_per_step": e2e_ms / args.steps,
@@ -411,6 +434,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, x, ids, w, gain, bank, shared, budget_s=args.cpu_budget,
                                               fp8=fp8)
+    del ws, shared_t
     return result
 
 
@@ -531,6 +555,8 @@ def main():
     ap.add_argument("--n-tokens", type=int, default=0,
                     help="override N (with --num-experts: a small case of the same rows per expert)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="default decode run only: skip the prefill sub-record")
     ap.add_argument("--act", default="exact", choices=["exact", "fp8"],
                     help="activation scheme: exact split terms (default) or dynamic FP8 (per-128 e4m3, amax/448)")
     args = ap.parse_args()

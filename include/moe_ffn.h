@@ -20,7 +20,10 @@
  *   - Buffers: all pointers except the dims/weights structs are DEVICE
  *     pointers owned by the caller.  The library never allocates or frees
  *     device memory and keeps no state between calls; scratch lives in the
- *     caller's workspace (see moe_workspace_size).
+ *     caller's workspace (see moe_workspace_size).  One exception:
+ *     moe_infer_static takes no workspace and uses a fixed array inside the
+ *     library that keeps the last call's contents (its Scratch and Sharing
+ *     notes below).
  *   - Layouts are dense row-major.  Sizes: n tokens, d model width, d_ff
  *     expert width, E experts, k experts per token, R = n * k routed rows.
  *   - Types: activations bf16 (uint16 bit patterns), expert rows f16,
@@ -76,9 +79,13 @@ typedef enum {
 
 /* Activation schemes ("Input features" page, quantisation config: fmt e4m3,
  * activation_scheme "dynamic", weight blocks of 128 x 128).
- *   MOE_ACT_EXACT        every activation row is carried exactly as e4m3
- *                        split terms (see Precision above); the result is
- *                        the unquantised function of the FP8 weights.
+ *   MOE_ACT_EXACT        activations are never quantised: every row is
+ *                        carried as e4m3 split terms (see Precision above),
+ *                        exact for bf16 values within 2^10 of their block's
+ *                        maximum (smaller ones within 2^-18 of it) and about
+ *                        12 significant bits for h, so the result is the
+ *                        function of the FP8 weights to within those
+ *                        roundings and the f16 rows.
  *   MOE_ACT_FP8_DYNAMIC  every row entering a linear (x, the normalised row,
  *                        h) is quantised on the fly per group of 128
  *                        features: scale s = amax / 448 in fp32 (1 for an
@@ -259,9 +266,11 @@ moe_status moe_mlp_forward(const moe_dims *dims, int64_t n_tokens, const void *x
  *   whose moe_workspace_size(dims, n, 0) exceeds it are rejected with
  *   MOE_ERR_WORKSPACE before anything runs (at K2 sizes, d 7168 / d_ff 2048 /
  *   k 8, that allows up to 24 tokens).
- *   Set-up: the first call on each device looks the array's device address up
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  No call allocates or frees memory.
+ *   Set-up: the first call in each device's CUDA context looks the array's
+ *   device address up (cudaGetSymbolAddress) with that device current and
+ *   remembers it for that context; make that first call before any stream
+ *   capture (after cudaDeviceReset the new context's first call looks it up
+ *   again).  No call allocates or frees memory.
  *   Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents; calls that can overlap on the GPU (different streams
  *   without ordering, several host threads) race and corrupt each other's

@@ -367,25 +367,59 @@ moe_status shared_pass(const moe_dims* d, int64_t n, const moe_weights* w, int32
 // library reserves it until the process exits.  Host code must not pass the
 // symbol itself to a kernel (on the host it only names a stand-in object); the
 // device address comes from cudaGetSymbolAddress below.
-#define MOE_STATIC_SCRATCH_BYTES_VALUE (size_t(8) << 20)
-static __device__ __align__(256) uint8_t moe_static_scratch[MOE_STATIC_SCRATCH_BYTES_VALUE];
+static __device__ __align__(256) uint8_t moe_static_scratch[MOE_STATIC_SCRATCH_BYTES];
 
 namespace {
 
-// Device address of moe_static_scratch on the current device, looked up once per
-// device (with that device current) and remembered; nullptr if the lookup fails.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0
+// when there is none or the driver does not offer the call.  Ids are never
+// reused within a process, unlike context handles and device indices.
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of moe_static_scratch in the current device's context.  It is
+// looked up (cudaGetSymbolAddress, with that device current) on the first call
+// in each context and remembered with the context's id, so a context created
+// again after cudaDeviceReset gets a fresh lookup instead of a stale address.
+// nullptr if the lookup fails.
 void* static_scratch_address() {
+  struct Entry {
+    unsigned long long ctx_id;
+    void* addr;
+  };
   static std::mutex mu;
-  static void* addr[64] = {};
+  static Entry cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, moe_static_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  if (id != 0 && cache[dev].ctx_id == id && cache[dev].addr) return cache[dev].addr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, moe_static_scratch) != cudaSuccess) return nullptr;
+  // the lookup creates the context if this thread had none yet: key the entry on it
+  cache[dev] = Entry{current_context_id(), p};
+  return p;
 }
 
 }  // namespace
@@ -617,14 +651,13 @@ moe_status moe_infer_static(const moe_dims* dims, int64_t n, const void* x, cons
   if (!dims || n < 0) return MOE_ERR_INVALID_ARG;
   Layout L;
   if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
-  if (L.total > MOE_STATIC_SCRATCH_BYTES_VALUE) return MOE_ERR_WORKSPACE;  // problem too big for the scratch
+  if (L.total > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;  // problem too big for the scratch
   if (n == 0) return MOE_OK;
   void* ws = static_scratch_address();
   if (!ws) return MOE_ERR_CUDA;
   // The same sequence as moe_infer; its first kernel resets the error word, the
   // only part of the scratch that must start at zero.
-  return moe_infer(dims, n, x, topk_ids, topk_weight, w, out, out_is_fp32, ws, MOE_STATIC_SCRATCH_BYTES_VALUE, s,
-                   nullptr);
+  return moe_infer(dims, n, x, topk_ids, topk_weight, w, out, out_is_fp32, ws, MOE_STATIC_SCRATCH_BYTES, s, nullptr);
 }
 
 moe_status moe_check_bounded_wait(void* ws, cudaStream_t s) {

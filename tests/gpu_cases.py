@@ -51,15 +51,41 @@ def workload(name_or_wl, n_tokens=None, ids=None) -> Case:
                 inp.gain.cuda() if inp.gain is not None else None, shared)
 
 
-def sample_tokens(ids: torch.Tensor, n_random: int, n_hot: int, seed: int = 0):
-    """Token subset for the oracle: n_random uniform tokens, n_hot tokens of the most loaded expert,
-    the first and the last token."""
-    n = ids.shape[0]
+def parity_tokens(ids: torch.Tensor, n_min: int = 512, top: int = 3, tile: int = 128, seed: int = 0):
+    """Token subset of a K2-sized batch that the oracle computes one by one (at least n_min tokens):
+
+    * one token of every expert that the batch selects (a greedy cover: a token covers its k experts),
+      so every expert's slice of both grouped GEMMs is compared;
+    * the tokens at the first and the last row of every `tile`-row tile of the `top` most-loaded experts,
+      in the sorted order (stable by expert, then flat index t * k + j), so every tile boundary of the
+      experts that span several tiles is compared;
+    * the first and the last token of the batch;
+    * seeded uniform tokens until n_min are picked."""
+    ids = ids.cpu().long()
+    n, k = ids.shape
     g = torch.Generator().manual_seed(seed)
-    pick = set(torch.randperm(n, generator=g)[:n_random].tolist())
-    counts = torch.bincount(ids.reshape(-1).long().cpu(), minlength=int(ids.max()) + 1)
-    hot = int(counts.argmax())
-    hot_tokens = (ids.cpu() == hot).any(dim=1).nonzero().flatten()
-    pick |= set(hot_tokens[torch.randperm(hot_tokens.numel(), generator=g)[:n_hot]].tolist())
-    pick |= {0, n - 1}
+    pick = {0, n - 1}
+    flat = ids.reshape(-1)
+    E = int(flat.max()) + 1
+    counts = torch.bincount(flat, minlength=E)
+    # every touched expert, in a seeded order; a token already picked may cover it
+    covered = torch.zeros(E, dtype=torch.bool)
+    for t in pick:
+        covered[ids[t]] = True
+    for e in torch.randperm(E, generator=g).tolist():
+        if counts[e] == 0 or covered[e]:
+            continue
+        toks = (ids == e).any(dim=1).nonzero().flatten()
+        t = int(toks[int(torch.randint(toks.numel(), (1,), generator=g))])
+        pick.add(t)
+        covered[ids[t]] = True
+    # first and last row of every tile of the most-loaded experts
+    for e in torch.argsort(counts, descending=True, stable=True)[:top].tolist():
+        rows = (flat == e).nonzero().flatten()       # ascending flat index = the stable sorted order
+        c = rows.numel()
+        for r0 in range(0, c, tile):
+            for r in (r0, min(r0 + tile - 1, c - 1)):
+                pick.add(int(rows[r]) // k)
+    rest = [t for t in torch.randperm(n, generator=g).tolist() if t not in pick]
+    pick.update(rest[:max(0, n_min - len(pick))])
     return sorted(pick)

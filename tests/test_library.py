@@ -132,3 +132,14 @@ def test_permute_rejects_a_workspace_shorter_than_its_prefix(lib):
     st = lib.moe_permute(ctypes.byref(dm), n, dummy, dummy, dummy, dummy, None, 0, ctypes.c_void_p(addr), need - 1,
                          None)
     assert st == 3
+
+
+def test_static_scratch_size_matches_header():
+    # the binding's copy of the built-in scratch size is the header's macro, the one the library is built with
+    text = open(os.path.join(ROOT, "include", "moe_ffn.h")).read()
+    m = re.search(r"#define\s+MOE_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "MOE_STATIC_SCRATCH_BYTES not found"
+    assert mx.MOE_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+    # K2 sizes: 24 tokens fit, 25 do not
+    dm = mx.dims(7168, 2048, 384, 8)
+    assert mx.moe_workspace_size(dm, 24) <= mx.MOE_STATIC_SCRATCH_BYTES < mx.moe_workspace_size(dm, 25)

@@ -4,10 +4,13 @@ Some callers cannot allocate device memory themselves (a plugin or embedded
 runtime that only hands over input and output buffers, code running inside
 another library's allocator hooks, paths where a cudaMalloc could synchronise
 the device).  For them the library offers moe_infer_static, which needs no
-workspace.  These tests call it through the C ABI and compare it with
-moe_infer (caller-provided workspace) on two calls in a row, under the same
-tolerance the parity tests use.  The file sorts last so that a run stopping at
-its first failure has run every other test; it also passes on its own.
+workspace.  These tests call it through the C ABI on two calls in a row and
+compare each result with moe_infer (caller-provided workspace): both run the
+same deterministic kernels on the same inputs, so the outputs must be equal
+bit for bit (leftover or partly overwritten scratch would show up here), and
+both must lie within the parity tolerance of the oracle.  The file sorts last
+so that a run stopping at its first failure has run every other test; it also
+passes on its own.
 """
 
 import pytest
@@ -31,8 +34,7 @@ def _static(c, x, ids, w):
 
 
 def _check_same(a, b):
-    rep = oracle.parity_report(a, b.double().cpu().numpy(), bf16_output=True)
-    assert rep["ok"], rep
+    assert torch.equal(a, b)
 
 
 def test_static_matches_workspace_entry_two_calls_tiny():
@@ -46,6 +48,12 @@ def test_static_matches_workspace_entry_two_calls_tiny():
     torch.cuda.synchronize()
     _check_same(a1, mx.infer(c.x, c.ids, c.w, c.bank))
     _check_same(a2, mx.infer(x2, ids2, w2, c.bank))
+    # and both against the oracle, under the parity tolerance
+    ref1 = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
+    ref2 = oracle.moe_infer(x2.cpu(), ids2.cpu(), w2.cpu(), c.inp.bank)
+    for y, ref in ((a1, ref1), (a2, ref2)):
+        rep = oracle.parity_report(y, ref, bf16_output=True)
+        assert rep["ok"], rep
 
 
 def test_static_matches_workspace_entry_two_calls_k2_decode():
@@ -56,6 +64,16 @@ def test_static_matches_workspace_entry_two_calls_k2_decode():
     torch.cuda.synchronize()
     _check_same(a1, mx.infer(c.x, c.ids, c.w, c.bank))
     _check_same(a2, mx.infer(x2, ids2, w2, c.bank))
+
+
+def test_static_k2_largest_batch_that_fits():
+    # 24 tokens is the largest K2 batch whose workspace fits the built-in scratch
+    dm = mx.dims(7168, 2048, 384, 8)
+    assert mx.moe_workspace_size(dm, 24) <= mx.MOE_STATIC_SCRATCH_BYTES
+    c = cases.workload("k2_decode", n_tokens=24)
+    a = _static(c, c.x, c.ids, c.w)
+    torch.cuda.synchronize()
+    _check_same(a, mx.infer(c.x, c.ids, c.w, c.bank))
 
 
 def test_static_rejects_problems_larger_than_its_scratch():
