@@ -148,6 +148,22 @@ bool map_act_planar(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Wide tiles of the exact scheme: f16 values in panels of 64 columns,
+// [K/64][rows][64]; box 64 (128 bytes) x box_rows x 2 panels, 128-byte
+// swizzle, so one copy brings a K block of 128 columns; rows past the end read
+// as zero.
+bool map_rows_f16(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, rows, K / 64};
+  const cuuint64_t strides[2] = {128, 128 * rows};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The split layout of `rows` sorted rows of width K, as the tile width chosen for
 // `rows` rows over `experts` experts reads it.
 SplitLayout rows_layout(int64_t rows, int64_t experts, int64_t K, int terms, bool fp8) {
@@ -223,14 +239,16 @@ struct Tracer {
   } while (0)
 
 // Activation map of one GEMM pass: the 3-D map of 16-token tiles (rows
-// interleaved with their term slots, box of 16 rows x the live terms), or the
-// planar map of wide tiles (box of 128 rows x all terms).
+// interleaved with their term slots, box of 16 rows x the live terms), the f16
+// rows of wide tiles (box of 128 rows x 64 values), or the planar FP8 codes of
+// wide tiles (box of 128 rows x all terms).
 struct ActMaps {
   CUtensorMap m16;
   CUtensorMap box;
-  bool make(bool wide, const void* base, uint64_t K, uint64_t rows, int terms) {
+  bool make(bool wide, bool fp8, const void* base, uint64_t K, uint64_t rows, int terms) {
     if (!wide) return map_act(&m16, base, K, rows, terms, kNTokSmall);
-    if (!map_act_planar(&box, base, K, rows, terms, kNTokWide)) return false;
+    if (!(fp8 ? map_act_planar(&box, base, K, rows, terms, kNTokWide) : map_rows_f16(&box, base, K, rows, kNTokWide)))
+      return false;
     m16 = box;
     return true;
   }
@@ -254,7 +272,7 @@ moe_status run_gemms(bool after_gather, bool fp8, const moe_weights* w, int64_t 
   const bool wide = ntok == kNTokWide;
   ActMaps mx, mh;
   const int h_terms = h_terms_of(fp8);
-  if (!mx.make(wide, xs, d, rows, x_terms) || !mh.make(wide, h, dff, rows, h_terms)) return MOE_ERR_CUDA;
+  if (!mx.make(wide, fp8, xs, d, rows, x_terms) || !mh.make(wide, fp8, h, dff, rows, h_terms)) return MOE_ERR_CUDA;
   CUtensorMap m_g, m_u, m_d;
   m_g = m_u = m_d = mx.m16;  // placeholders when the bank is tiled
   if (!map_bank(w, d, dff, experts, &m_g, &m_u, &m_d)) return MOE_ERR_CUDA;

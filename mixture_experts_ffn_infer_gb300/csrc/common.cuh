@@ -71,24 +71,34 @@ __host__ __device__ constexpr int tile_tokens(int64_t rows, int64_t experts) {
   return rows >= 24 * experts ? kNTokWide : kNTokSmall;
 }
 
-// Where the split-format codes of a sorted row live (split3.cuh): term t of
-// row i starts at base + i * row_stride + t * term_stride bytes.
-//   16-token tiles: rows interleaved with three term slots, [rows][3][K]
-//                   (row_stride 3K, term_stride K; the live terms first)
-//   wide tiles:     one plane per term, [terms][rows][K]
-//                   (row_stride K, term_stride rows * K, 1 to 3 terms)
-// fp8 != 0: the dynamic FP8 scheme, one e4m3 term per value with the scale
-// amax / 448 per 128 columns (the first slot of the 16-token layout, or one
-// plane of the wide layout).
+// Where the sorted activation rows live and in which format.
+//   16-token tiles: e4m3 split-format codes (split3.cuh), rows interleaved
+//                   with three term slots, [rows][3][K] (row_stride 3K,
+//                   term_stride K; the live terms first)
+//   wide tiles:     f16 values in panels of 64 columns, [K/64][rows][64]
+//                   (row_stride 128 bytes within a panel, term_stride =
+//                   rows * 128 bytes between panels), so that one TMA box
+//                   brings a K block of 128 columns of a tile as two 16 KB
+//                   panels; each row is divided by a power of two of its own
+//                   (kept in the factor array, one per row), so a bf16 value
+//                   is held exactly
+//   fp8 != 0:       the dynamic FP8 scheme, one e4m3 term per value with the
+//                   scale amax / 448 per 128 columns (the first slot of the
+//                   16-token layout, or one plane [rows][K] for wide tiles)
+// The factor array holds, per (128 columns, row), 2^-s of the split format or
+// the FP8 scale ([K/128][rows]); for f16 rows, per row, the power of two to
+// multiply the row by ([rows]).
 struct SplitLayout {
   int64_t row_stride;
   int64_t term_stride;
   int32_t terms;
   int32_t fp8;
+  int32_t f16;
 };
 inline SplitLayout split_layout(bool wide, int64_t rows, int64_t K, int terms, bool fp8) {
+  if (wide && !fp8) return SplitLayout{128, rows * 128, 1, 0, 1};
   const int32_t t = fp8 ? 1 : terms, f = fp8 ? 1 : 0;
-  return wide ? SplitLayout{K, rows * K, t, f} : SplitLayout{3 * K, K, t, f};
+  return wide ? SplitLayout{K, rows * K, t, f, 0} : SplitLayout{3 * K, K, t, f, 0};
 }
 
 // Launch with programmatic stream serialization when `overlap`: the kernel may
@@ -150,7 +160,9 @@ struct GemmLaunch {
   const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
   const CUtensorMap* w1;        // up (gate/up pass only)
   const CUtensorMap* act;       // 16-token tiles: 3-D map over [rows][3][K] e4m3, box 128 x terms x 16
-  const CUtensorMap* act_box;   // wide tiles: 3-D map over [terms][rows][K], box 128 x 128 rows x terms
+  const CUtensorMap* act_box;   // wide tiles: f16 panels [K/64][rows][64], box 64 x 128 rows x 2 panels
+                                //   (exact scheme), or
+                                //   3-D map over [terms][rows][K], box 128 x 128 rows x terms (FP8)
   int32_t ntok;                 // token tile width (kNTokSmall or kNTokWide)
   int32_t terms;                // live activation terms per row (1 to 3)
   bool fp8;                     // dynamic FP8 activations: gate/up writes h as one e4m3 term, scale amax / 448
@@ -165,9 +177,10 @@ struct GemmLaunch {
   // A unit is one token tile times two weight blocks: gate/up pass = row block j
   // of w0 and of w1; down pass = row blocks 2j and 2j + 1 of w0.
   int32_t num_kb;               // K / 128
-  const float* act_inv;         // [num_kb][act_rows] factor of each activation block (2^-s, or the FP8 scale)
+  const float* act_inv;         // [num_kb][act_rows] factor of each activation block (2^-s, or the FP8 scale);
+                                //   f16 rows: [act_rows] power of two of each row (NULL = 1)
   int32_t act_rows;             // rows of the sorted activation matrix
-  void* out;                    // gate/up: h codes (layout of the next pass); down: rows [.][n_nb*128] f16
+  void* out;                    // gate/up: h (layout of the next pass); down: rows [.][n_nb*128] f16
   float* out_inv;               // gate/up: [n_nb][act_rows] factor of each h block
   const int32_t* sorted_pos;    // down: flat position of each sorted row (NULL = identity)
   const float* topk_weight;     // down: flat router weights (NULL = 1)
@@ -178,7 +191,11 @@ struct GemmLaunch {
 };
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s);
-// moe_gemm_wide.cu (the two above forward wide tiles here)
+// moe_gemm_f16.cu (the two above forward wide tiles of the exact scheme here):
+// f16 token rows, weights converted to f16 with their block scale on chip
+cudaError_t launch_gateup_f16(const GemmLaunch& g, cudaStream_t s);
+cudaError_t launch_down_f16(const GemmLaunch& g, cudaStream_t s);
+// moe_gemm_wide.cu (wide tiles of the dynamic FP8 scheme)
 cudaError_t launch_gateup_wide(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_down_wide(const GemmLaunch& g, cudaStream_t s);
 

@@ -2,15 +2,21 @@
 //
 // gather_rows_kernel    - "Mixture of experts" page, moe_infer: sorted_tokens
 //                         = x[idxs // k]; each token's row is split once into
-//                         the e4m3 split format the GEMMs read (split3.cuh), or
-//                         quantised to dynamic FP8, and written to all of its
-//                         sorted positions.
+//                         the e4m3 split format the 16-token GEMMs read
+//                         (split3.cuh), or quantised to dynamic FP8, and written
+//                         to all of its sorted positions.
+// gather_rows_f16_kernel- the same gather for the wide f16 GEMMs: the row is
+//                         divided by a power of two of its own (its largest
+//                         magnitude lands in [2^14, 2^15)) and stored as f16,
+//                         which holds every bf16 value of the row exactly
+//                         unless it lies more than 2^28 below the maximum.
 // rmsnorm_scatter_kernel- "Input features" page, RMSNorm: fp32 mean of squares,
 //                         h / sqrt(mean + eps) cast to bf16, times the bf16 gain
 //                         in bf16; the normalised row is split once (two terms
-//                         hold a bf16 value) and written per routed slot straight
-//                         to its sorted position (inv_pos) and to the shared
-//                         expert's rows.
+//                         hold a bf16 value) or stored as scaled f16 (as the f16
+//                         gather), and written per routed slot straight to its
+//                         sorted position (inv_pos) and to the shared expert's
+//                         rows.
 // pack_tiles_kernel     - storage layout only: copies each 128 x 128 tile of
 //                         e4m3 codes into one contiguous 16 KB block, laid out
 //                         exactly as a 128-byte-swizzled TMA box lands in
@@ -44,6 +50,37 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
 }
 
 constexpr int kRowThreads = 256;  // eight warps per row, one 128-column block per warp at a time
+
+// The power of two s of an f16 row whose largest magnitude is m: m * 2^-s lies
+// in [2^14, 2^15), inside f16's range with 28 binades of normal numbers below
+// it.  0 for an all-zero or non-finite row; limited to [-126, 113] so that 2^s
+// and 2^-s stay normal floats.
+__device__ __forceinline__ int f16_row_exponent(float m) {
+  if (!(m > 0.f) || !(m < 3.0e38f)) return 0;
+  int e;
+  frexpf(m, &e);  // m = f * 2^e, f in [0.5, 1)
+  return max(-126, min(113, e - 15));
+}
+
+// Largest value over the CTA (kRowThreads threads; every thread gets it).
+__device__ __forceinline__ float block_max(float m, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __syncthreads();  // red may still be read from an earlier use
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kRowThreads / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// Four values times 2^-s as f16 (exact for bf16 inputs in range), packed in two words.
+__device__ __forceinline__ uint2 f16x4_scaled(const float (&v)[4], int s) {
+  const __half2 a = __floats2half2_rn(ldexpf(v[0], -s), ldexpf(v[1], -s));
+  const __half2 b = __floats2half2_rn(ldexpf(v[2], -s), ldexpf(v[3], -s));
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
 
 // One CTA per token and column group (blockIdx.y of gridDim.y, a batch with
 // fewer tokens than SMs spreads each row over several CTAs): the token's row is
@@ -89,6 +126,44 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
       for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
     }
   }
+}
+
+// One CTA per token: the row's largest magnitude, then the row as f16 times
+// 2^-s to every sorted position of the token, and 2^s to the factor array.
+__global__ void __launch_bounds__(kRowThreads) gather_rows_f16_kernel(const uint16_t* __restrict__ x,
+                                                                      const int32_t* __restrict__ inv_pos,
+                                                                      int32_t n, int32_t k, int32_t d,
+                                                                      uint8_t* __restrict__ xs, SplitLayout lay,
+                                                                      float* __restrict__ xs_scale) {
+  __shared__ float red[kRowThreads / 32];
+  pdl_wait();  // launched behind the routing plan, whose inv_pos it reads
+  pdl_launch_dependents();
+  const int64_t t = blockIdx.x;
+  const int64_t R = static_cast<int64_t>(n) * k;
+  int32_t dst_rows[32];
+  int ndst = 0;
+  for (int j = 0; j < k; ++j) {
+    const int p = inv_pos ? inv_pos[t * k + j] : static_cast<int>(t * k + j);  // null: identity order
+    if (p >= 0 && p < R) dst_rows[ndst++] = p;
+  }
+  if (ndst == 0) return;  // the whole CTA leaves together (ndst is the same for every thread)
+  const uint2* src = reinterpret_cast<const uint2*>(x + t * d);  // four bf16 per uint2
+  const int nq = d / 4;
+  float m = 0.f;
+  for (int c = threadIdx.x; c < nq; c += kRowThreads) {
+    const uint2 w = src[c];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))), fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
+  }
+  const int s = f16_row_exponent(block_max(m, red));
+  for (int c = threadIdx.x; c < nq; c += kRowThreads) {
+    const uint2 w = src[c];
+    const float v[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+    const uint2 o = f16x4_scaled(v, s);
+    // columns 4c..4c+3: panel c / 16, bytes (c % 16) * 8 of the row's 128 in it
+    uint8_t* panel = xs + static_cast<int64_t>(c >> 4) * lay.term_stride + (c & 15) * 8;
+    for (int q = 0; q < ndst; ++q) *reinterpret_cast<uint2*>(panel + static_cast<int64_t>(dst_rows[q]) * lay.row_stride) = o;
+  }
+  if (threadIdx.x < ndst) xs_scale[dst_rows[threadIdx.x]] = ldexpf(1.0f, s);
 }
 
 // inv[sorted_pos[i]] = i for every valid entry; the rest stay -1 (set before).
@@ -139,20 +214,52 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_scatter_kernel(
     if (p >= 0) dst_rows[ndst++] = p;
   }
   const int64_t R = static_cast<int64_t>(n) * k;
-  for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
+  // the normalised row is cast to bf16, then multiplied by the bf16 gain in bf16
+  auto normalised = [&](int kb, float (&v)[4]) {
     const uint2 w = reinterpret_cast<const uint2*>(h + t * d + kb * 128)[lane];
     const uint2 g = reinterpret_cast<const uint2*>(gain + kb * 128)[lane];
-    // the normalised row is cast to bf16, then multiplied by the bf16 gain in bf16
-    float v[4];
     v[0] = bf16_round(bf16_lo(g.x) * bf16_round(bf16_lo(w.x) * inv_rms));
     v[1] = bf16_round(bf16_hi(g.x) * bf16_round(bf16_hi(w.x) * inv_rms));
     v[2] = bf16_round(bf16_lo(g.y) * bf16_round(bf16_lo(w.y) * inv_rms));
     v[3] = bf16_round(bf16_hi(g.y) * bf16_round(bf16_hi(w.y) * inv_rms));
-    uint32_t t1, t2, t3;
-    const float inv = lay.fp8 ? warp_fp8_block(v, t1, t2, t3) : warp_split_block(v, t1, t2, t3);
-    for (int q = 0; q < ndst; ++q) warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
-    if (xs_shared) warp_store_block(xs_shared, lay_shared, xs_shared_inv, n, t, kb, t1, t2, t3, inv, lane);
+  };
+  // f16 rows (wide tiles) need the normalised row's largest magnitude first
+  int s = 0;
+  if (lay.f16 || (xs_shared && lay_shared.f16)) {
+    float m = 0.f;
+    for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
+      float v[4];
+      normalised(kb, v);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    }
+    s = f16_row_exponent(block_max(m, red));
   }
+  for (int kb = warp; kb < d / 128; kb += kRowThreads / 32) {
+    float v[4];
+    normalised(kb, v);
+    uint2 f16v = make_uint2(0u, 0u);
+    if (lay.f16 || (xs_shared && lay_shared.f16)) f16v = f16x4_scaled(v, s);
+    uint32_t t1 = 0, t2 = 0, t3 = 0;
+    float inv = 0.f;
+    if (!lay.f16 || (xs_shared && !lay_shared.f16))
+      inv = lay.fp8 || lay_shared.fp8 ? warp_fp8_block(v, t1, t2, t3) : warp_split_block(v, t1, t2, t3);
+    for (int q = 0; q < ndst; ++q) {
+      if (lay.f16)  // columns 4 lane.. of block kb: panel 2 kb + lane / 16
+        *reinterpret_cast<uint2*>(xs + static_cast<int64_t>(2 * kb + (lane >> 4)) * lay.term_stride +
+                                  static_cast<int64_t>(dst_rows[q]) * lay.row_stride + (lane & 15) * 8) = f16v;
+      else
+        warp_store_block(xs, lay, xs_inv, R, dst_rows[q], kb, t1, t2, t3, inv, lane);
+    }
+    if (xs_shared) {
+      if (lay_shared.f16)
+        *reinterpret_cast<uint2*>(xs_shared + static_cast<int64_t>(2 * kb + (lane >> 4)) * lay_shared.term_stride +
+                                  t * lay_shared.row_stride + (lane & 15) * 8) = f16v;
+      else
+        warp_store_block(xs_shared, lay_shared, xs_shared_inv, n, t, kb, t1, t2, t3, inv, lane);
+    }
+  }
+  if (lay.f16 && threadIdx.x < ndst) xs_inv[dst_rows[threadIdx.x]] = ldexpf(1.0f, s);
+  if (xs_shared && lay_shared.f16 && threadIdx.x == 0) xs_shared_inv[t] = ldexpf(1.0f, s);
 }
 
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows,
@@ -255,6 +362,19 @@ cudaError_t launch_pack_tiles(const uint8_t* src0, const uint8_t* src1, uint8_t*
 cudaError_t launch_gather_rows(const uint16_t* x_bf16, const int32_t* inv_pos, int32_t n, int32_t k, int32_t d,
                                uint8_t* xs, SplitLayout lay, float* xs_inv, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
+  if (lay.f16) {
+    // one CTA per token (its row's maximum is needed before any value is stored)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gather_rows_f16_kernel, x_bf16, inv_pos, n, k, d, xs, lay, xs_inv);
+  }
   // a batch smaller than the GPU spreads each row's column blocks over several CTAs
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=

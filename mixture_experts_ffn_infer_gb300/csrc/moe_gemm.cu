@@ -559,14 +559,14 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 //            three of 64 KB)
 // Wide tiles (up to 128 tokens) go to moe_gemm_wide.cu.
 cudaError_t launch_gateup(const GemmLaunch& g, cudaStream_t s) {
-  if (g.ntok == kNTokWide) return launch_gateup_wide(g, s);
+  if (g.ntok == kNTokWide) return g.fp8 ? launch_gateup_wide(g, s) : launch_gateup_f16(g, s);
   if (g.ntok != kNTokSmall) return cudaErrorInvalidValue;
   if (g.terms == 2) return launch_gemm<true, kNTokSmall, 2, 1, 6, 4, 4>(g, s);
   if (g.terms == 1) return launch_gemm<true, kNTokSmall, 1, 1, 6, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down(const GemmLaunch& g, cudaStream_t s) {
-  if (g.ntok == kNTokWide) return launch_down_wide(g, s);
+  if (g.ntok == kNTokWide) return g.fp8 ? launch_down_wide(g, s) : launch_down_f16(g, s);
   if (g.ntok != kNTokSmall) return cudaErrorInvalidValue;
   if (g.terms == 3) return launch_gemm<false, kNTokSmall, 3, 1, 5, 4, 4>(g, s);
   if (g.terms == 1) return launch_gemm<false, kNTokSmall, 1, 1, 5, 4, 4>(g, s);

@@ -566,18 +566,13 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
 
 }  // namespace
 
-// Stages: three weight stages of 32 KB (both blocks of one K block) and
-// activation stages of terms x 16 KB (three of 32 KB for the two terms of the
-// bf16 features, two of 48 KB for the three terms of h); about 195 KB of
-// shared memory.  Dynamic FP8 (one term): four weight stages and four 16 KB
-// activation stages, the same shared memory.
+// Stages (dynamic FP8, one term): four 32 KB weight stages (both blocks of one
+// K block) and four 16 KB activation stages; about 195 KB of shared memory.
 cudaError_t launch_gateup_wide(const GemmLaunch& g, cudaStream_t s) {
-  if (g.terms == 2 && !g.fp8) return launch_wide<true, 2, 3, 3>(g, s);
   if (g.terms == 1 && g.fp8) return launch_wide<true, 1, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down_wide(const GemmLaunch& g, cudaStream_t s) {
-  if (g.terms == 3 && !g.fp8) return launch_wide<false, 3, 3, 2>(g, s);
   if (g.terms == 1 && g.fp8) return launch_wide<false, 1, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
