@@ -255,6 +255,103 @@ moe_status moe_mlp_forward(const moe_dims *dims, int64_t n_tokens, const void *x
                            void *out, int32_t out_is_fp32, void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
+/* ---------------------------------------------------------------- expert parallelism
+ * "Input features" page, expert construction: with ep_size ranks, rank r holds
+ * the experts [r * E/ep, (r + 1) * E/ep) (experts_per_rank = E / ep_size).
+ * "Mixture of experts" page, moe_infer, ep_size > 1 branch: every rank sends
+ * the rows it routes to rank r's experts to rank r, each rank groups what it
+ * receives by local expert and runs its experts, the outputs return to their
+ * source ranks and each token sums its k rows weighted by topk_weight.
+ *
+ * The two exchanges (an all-to-all of the per-expert counts, then of the rows
+ * and back) are the caller's, e.g. NCCL through torch.distributed; the calls
+ * below are the steps on either side of them, all asynchronous on `stream`
+ * with no host synchronisation.  Rows travel in "slot" buffers:
+ *   capacity = 0  rows for rank d follow those for ranks < d without gaps
+ *                 (the pages' layout: the caller reads send_counts and the
+ *                 received counts back to size the exchange);
+ *   capacity = C  rows for rank d sit at slots d*C .. d*C + C - 1 (fixed split
+ *                 sizes C, nothing to read back; a rank routing more than C
+ *                 entries to one rank drops the rest and raises
+ *                 MOE_ERR_ROUTING).
+ * Sequence on each rank, for a batch of n tokens:
+ *   1. moe_ep_dispatch_plan -> tokens_per_expert, send_counts, tok_slot
+ *   2. moe_ep_gather        -> send rows (bf16, slot order)
+ *   3. exchange tokens_per_expert [E] with equal splits of E/ep: rank r gets
+ *      recv_counts [ep][E/ep] (source-major); exchange the rows
+ *   4. moe_ep_regroup       -> local expert offsets, row_pos, pos_row
+ *   5. moe_ep_experts_forward -> expert outputs in received slot order
+ *   6. exchange the outputs back (the reverse of step 3's row exchange)
+ *   7. moe_ep_combine       -> out [n, d]
+ * Device-detected errors land in the error word at the start of each call's
+ * workspace; moe_get_error reads it. */
+
+/* Bytes of workspace moe_ep_dispatch_plan needs for n tokens (0: unsupported). */
+size_t moe_ep_plan_workspace_size(const moe_dims *dims, int64_t n_tokens);
+
+/* Step 1: the rank's routing plan (count and stable sort, as moe_permute) and
+ * where each (token, slot) entry travels.
+ *   dims              the full model: E = all routed experts, E % ep_size == 0
+ *   ep_size           ranks, 1..256
+ *   topk_ids          [n, k] int32 in
+ *   tokens_per_expert [E] int32 out: entries per expert (what step 3 exchanges)
+ *   send_counts       [ep] int32 out: entries for each rank (its split size)
+ *   tok_slot          [n*k] int32 out: send slot of entry t*k+j, -1 when its id
+ *                     is outside [0, E) (MOE_ERR_ROUTING) or dropped over capacity
+ *   capacity          0 or C (see above) */
+moe_status moe_ep_dispatch_plan(const moe_dims *dims, int32_t ep_size, int64_t n_tokens, const int32_t *topk_ids,
+                                int32_t *tokens_per_expert, int32_t *send_counts, int32_t *tok_slot, int64_t capacity,
+                                void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 2: send_rows[tok_slot[t*k+j]] = x[t] for every entry with a slot.
+ *   x [n, d] bf16 in; send_rows [n_slots, d] bf16 out (slots without an entry are
+ *   left as they are); n_slots = the send buffer's rows (n*k, or ep*C). */
+moe_status moe_ep_gather(const moe_dims *dims, int64_t n_tokens, const void *x, const int32_t *tok_slot,
+                         int64_t n_slots, void *send_rows, cudaStream_t stream);
+
+/* Bytes of workspace moe_ep_regroup needs (0: unsupported sizes). */
+size_t moe_ep_regroup_workspace_size(int32_t experts_per_rank, int32_t ep_size);
+
+/* Step 4, on the receiving rank: the received rows grouped by local expert,
+ * ties in received order (the page's regroup, taken stable).
+ *   recv_counts   [ep][experts_per_rank] int32 in: rows from each source rank
+ *                 for each local expert, as the count exchange delivers them
+ *   capacity      0: the sources' rows follow each other without gaps; C: the
+ *                 rows from source r start at slot r*C
+ *   n_slots       rows of the received buffer; counts that do not fit are cut
+ *                 (MOE_ERR_ROUTING)
+ *   local_counts  [experts_per_rank] int32 out; local_offsets [experts_per_rank+1]
+ *   row_pos       [n_slots] int32 out: position of received slot i in expert
+ *                 order, -1 for an unused slot
+ *   pos_row       [n_slots] int32 out: its inverse on the used positions */
+moe_status moe_ep_regroup(int32_t experts_per_rank, int32_t ep_size, const int32_t *recv_counts, int64_t capacity,
+                          int64_t n_slots, int32_t *local_counts, int32_t *local_offsets, int32_t *row_pos,
+                          int32_t *pos_row, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 5: this rank's experts on the received rows ("SwiGLU output" page, MLP
+ * class, each expert on its contiguous slice).
+ *   dims          num_experts = experts_per_rank, top_k = 1 (else
+ *                 MOE_ERR_UNSUPPORTED), d, d_ff, act_scheme as for moe_infer
+ *   recv_rows     [n_slots, d] bf16 in (received slot order)
+ *   local_offsets, row_pos, pos_row: from moe_ep_regroup
+ *   weights       the rank's bank, E = experts_per_rank (global expert r*epr + e
+ *                 at index e)
+ *   out_rows      [n_slots, d] f16 out: expert(row) at the row's received slot,
+ *                 not weighted; unused slots are left as they are
+ *   workspace     moe_workspace_size(dims, n_slots, 0) bytes */
+moe_status moe_ep_experts_forward(const moe_dims *dims, int64_t n_slots, const void *recv_rows,
+                                  const int32_t *local_offsets, const int32_t *row_pos, const int32_t *pos_row,
+                                  const moe_weights *weights, void *out_rows, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/* Step 7: out[t] = sum_j topk_weight[t][j] * back_rows[tok_slot[t*k+j]] in fp32,
+ * j ascending (entries without a slot add nothing).
+ *   back_rows [n_slots, d] f16 in: the expert outputs returned to their send slots
+ *   out       [n, d] bf16, or fp32 when out_is_fp32 != 0 */
+moe_status moe_ep_combine(const moe_dims *dims, int64_t n_tokens, const void *back_rows, const int32_t *tok_slot,
+                          int64_t n_slots, const float *topk_weight, void *out, int32_t out_is_fp32,
+                          cudaStream_t stream);
+
 /* moe_infer without a workspace, for callers that cannot allocate device
  * memory themselves: code that only receives input and output buffers from a
  * host framework (a plugin or an embedded runtime with its own memory

@@ -89,6 +89,21 @@ _SIGS = {
                                        ctypes.c_size_t, ctypes.c_void_p]),
     "moe_infer_static": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 3
                          + [ctypes.POINTER(moe_weights), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "moe_ep_plan_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_dims), ctypes.c_int64]),
+    "moe_ep_dispatch_plan": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int32, ctypes.c_int64]
+                             + [ctypes.c_void_p] * 4 + [ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                                        ctypes.c_void_p]),
+    "moe_ep_gather": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_ep_regroup_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
+    "moe_ep_regroup": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_int64] + [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_ep_experts_forward": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64] + [ctypes.c_void_p] * 4
+                               + [ctypes.POINTER(moe_weights), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                  ctypes.c_void_p]),
+    "moe_ep_combine": (ctypes.c_int, [ctypes.POINTER(moe_dims), ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                      ctypes.c_void_p]),
     "moe_check_bounded_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_get_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
 }
@@ -226,6 +241,50 @@ def moe_infer_static(dm, n_tokens, x, topk_ids, topk_weight, w: moe_weights, out
     st = load_library().moe_infer_static(ctypes.byref(dm), n_tokens, _ptr(x), _ptr(topk_ids), _ptr(topk_weight),
                                          ctypes.byref(w), _ptr(out), int(bool(out_is_fp32)), _stream(stream))
     _check(st, "moe_infer_static")
+
+
+def moe_ep_plan_workspace_size(dm: moe_dims, n_tokens: int) -> int:
+    return load_library().moe_ep_plan_workspace_size(ctypes.byref(dm), n_tokens)
+
+
+def moe_ep_dispatch_plan(dm, ep_size, n_tokens, topk_ids, tokens_per_expert, send_counts, tok_slot, capacity, ws,
+                         stream=None):
+    st = load_library().moe_ep_dispatch_plan(ctypes.byref(dm), ep_size, n_tokens, _ptr(topk_ids),
+                                             _ptr(tokens_per_expert), _ptr(send_counts), _ptr(tok_slot), capacity,
+                                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "moe_ep_dispatch_plan")
+
+
+def moe_ep_gather(dm, n_tokens, x, tok_slot, n_slots, send_rows, stream=None):
+    st = load_library().moe_ep_gather(ctypes.byref(dm), n_tokens, _ptr(x), _ptr(tok_slot), n_slots, _ptr(send_rows),
+                                      _stream(stream))
+    _check(st, "moe_ep_gather")
+
+
+def moe_ep_regroup_workspace_size(experts_per_rank: int, ep_size: int) -> int:
+    return load_library().moe_ep_regroup_workspace_size(experts_per_rank, ep_size)
+
+
+def moe_ep_regroup(experts_per_rank, ep_size, recv_counts, capacity, n_slots, local_counts, local_offsets, row_pos,
+                   pos_row, ws, stream=None):
+    st = load_library().moe_ep_regroup(experts_per_rank, ep_size, _ptr(recv_counts), capacity, n_slots,
+                                       _ptr(local_counts), _ptr(local_offsets), _ptr(row_pos), _ptr(pos_row),
+                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "moe_ep_regroup")
+
+
+def moe_ep_experts_forward(dm, n_slots, recv_rows, local_offsets, row_pos, pos_row, w: moe_weights, out_rows, ws,
+                           stream=None):
+    st = load_library().moe_ep_experts_forward(ctypes.byref(dm), n_slots, _ptr(recv_rows), _ptr(local_offsets),
+                                               _ptr(row_pos), _ptr(pos_row), ctypes.byref(w), _ptr(out_rows),
+                                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "moe_ep_experts_forward")
+
+
+def moe_ep_combine(dm, n_tokens, back_rows, tok_slot, n_slots, topk_weight, out, out_is_fp32=False, stream=None):
+    st = load_library().moe_ep_combine(ctypes.byref(dm), n_tokens, _ptr(back_rows), _ptr(tok_slot), n_slots,
+                                       _ptr(topk_weight), _ptr(out), int(bool(out_is_fp32)), _stream(stream))
+    _check(st, "moe_ep_combine")
 
 
 def moe_check_bounded_wait(ws, stream=None):

@@ -17,6 +17,7 @@ namespace {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+constexpr int kMaxEpRanks = 256;  // ranks of an expert-parallel group
 
 // ---------------------------------------------------------------- workspace
 // Sorted activations and h are kept in the split format (split3.cuh): e4m3
@@ -240,21 +241,31 @@ struct Tracer {
 
 // Activation map of one GEMM pass: the 3-D map of 16-token tiles (rows
 // interleaved with their term slots, box of 16 rows x the live terms), the f16
-// rows of wide tiles (box of 128 rows x 64 values), or the planar FP8 codes of
-// wide tiles (box of 128 rows x all terms).
+// panels of wide tiles (boxes of 32, 64, 96 and 128 rows x 64 values x two
+// panels, so a tile's copy brings only its own rows rounded up to 32), or the
+// planar FP8 codes of wide tiles (box of 128 rows x all terms).
 struct ActMaps {
   CUtensorMap m16;
   CUtensorMap box;
+  CUtensorMap box_rows[3];
+  bool f16 = false;
   bool make(bool wide, bool fp8, const void* base, uint64_t K, uint64_t rows, int terms) {
     if (!wide) return map_act(&m16, base, K, rows, terms, kNTokSmall);
-    if (!(fp8 ? map_act_planar(&box, base, K, rows, terms, kNTokWide) : map_rows_f16(&box, base, K, rows, kNTokWide)))
-      return false;
+    if (fp8) {
+      if (!map_act_planar(&box, base, K, rows, terms, kNTokWide)) return false;
+    } else {
+      f16 = true;
+      for (int i = 0; i < 3; ++i)
+        if (!map_rows_f16(&box_rows[i], base, K, rows, 32 * (i + 1))) return false;
+      if (!map_rows_f16(&box, base, K, rows, kNTokWide)) return false;
+    }
     m16 = box;
     return true;
   }
   void bind(GemmLaunch& g) const {
     g.act = &m16;
     g.act_box = &box;
+    for (int i = 0; i < 3; ++i) g.act_box_rows[i] = f16 ? &box_rows[i] : nullptr;
   }
 };
 
@@ -676,6 +687,118 @@ moe_status moe_infer_static(const moe_dims* dims, int64_t n, const void* x, cons
   // The same sequence as moe_infer; its first kernel resets the error word, the
   // only part of the scratch that must start at zero.
   return moe_infer(dims, n, x, topk_ids, topk_weight, w, out, out_is_fp32, ws, MOE_STATIC_SCRATCH_BYTES, s, nullptr);
+}
+
+// ---------------------------------------------------------------- expert parallelism
+
+size_t moe_ep_plan_workspace_size(const moe_dims* dims, int64_t n_tokens) {
+  Layout L;
+  if (!make_layout(dims, n_tokens, 0, &L)) return 0;
+  return L.xs;  // the error word, routing scratch, counts, offsets, sorted_pos and inv_pos
+}
+
+moe_status moe_ep_dispatch_plan(const moe_dims* dims, int32_t ep_size, int64_t n, const int32_t* topk_ids,
+                                int32_t* tokens_per_expert, int32_t* send_counts, int32_t* tok_slot, int64_t capacity,
+                                void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!dims || n < 0 || capacity < 0) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(dims, n, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (ep_size < 1 || ep_size > kMaxEpRanks || dims->num_experts % ep_size != 0) return MOE_ERR_UNSUPPORTED;
+  if (capacity * ep_size >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.xs) return MOE_ERR_WORKSPACE;
+  if (!tokens_per_expert || !send_counts) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!topk_ids || !tok_slot)) return MOE_ERR_INVALID_ARG;
+  const int32_t R = static_cast<int32_t>(n * dims->top_k);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* ip = at<int32_t>(ws, L.inv_pos);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  if (launch_route_permute(topk_ids, static_cast<int32_t>(n), dims->top_k, dims->num_experts, tokens_per_expert,
+                           offsets, at<int32_t>(ws, L.sorted_pos), ip, 0, at<int32_t>(ws, L.route), err, 0, nullptr,
+                           nullptr, s) != cudaSuccess ||
+      launch_ep_send_plan(topk_ids, R, dims->num_experts, ep_size, offsets, ip, capacity, send_counts, tok_slot, err,
+                          s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_ep_gather(const moe_dims* dims, int64_t n, const void* x, const int32_t* tok_slot, int64_t n_slots,
+                         void* send_rows, cudaStream_t s) {
+  if (!dims || n < 0 || n_slots < 0) return MOE_ERR_INVALID_ARG;
+  if (!dims_ok(dims) || n * dims->top_k >= (int64_t(1) << 31) || n_slots >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (n == 0) return MOE_OK;
+  if (!x || !tok_slot || !send_rows || !aligned(x, 16) || !aligned(send_rows, 16)) return MOE_ERR_INVALID_ARG;
+  if (launch_ep_gather(static_cast<const uint16_t*>(x), tok_slot, static_cast<int32_t>(n), dims->top_k, dims->d,
+                       n_slots, static_cast<uint16_t*>(send_rows), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+size_t moe_ep_regroup_workspace_size(int32_t experts_per_rank, int32_t ep_size) {
+  if (experts_per_rank < 1 || ep_size < 1 || ep_size > kMaxEpRanks ||
+      static_cast<int64_t>(experts_per_rank) * ep_size > kMaxExperts)
+    return 0;
+  return 256 + align_up(4 * static_cast<size_t>(ep_regroup_scratch_ints(experts_per_rank, ep_size)));
+}
+
+moe_status moe_ep_regroup(int32_t epr, int32_t ep_size, const int32_t* recv_counts, int64_t capacity, int64_t n_slots,
+                          int32_t* local_counts, int32_t* local_offsets, int32_t* row_pos, int32_t* pos_row, void* ws,
+                          size_t ws_bytes, cudaStream_t s) {
+  if (capacity < 0 || n_slots < 0) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_ep_regroup_workspace_size(epr, ep_size);
+  if (need == 0 || n_slots >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (!recv_counts || !local_counts || !local_offsets || (n_slots > 0 && (!row_pos || !pos_row)))
+    return MOE_ERR_INVALID_ARG;
+  if (launch_ep_regroup(recv_counts, epr, ep_size, capacity, n_slots, local_counts, local_offsets, row_pos, pos_row,
+                        at<int32_t>(ws, 256), static_cast<uint32_t*>(ws), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_ep_experts_forward(const moe_dims* dims, int64_t n_slots, const void* recv_rows,
+                                  const int32_t* local_offsets, const int32_t* row_pos, const int32_t* pos_row,
+                                  const moe_weights* w, void* out_rows, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!dims || n_slots < 0) return MOE_ERR_INVALID_ARG;
+  if (dims->top_k != 1) return MOE_ERR_UNSUPPORTED;
+  Layout L;
+  if (!make_layout(dims, n_slots, 0, &L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (n_slots == 0) return MOE_OK;
+  if (!recv_rows || !local_offsets || !row_pos || !pos_row || !out_rows || !weights_ok(w) || !aligned(recv_rows, 16) ||
+      !aligned(out_rows, 16))
+    return MOE_ERR_INVALID_ARG;
+  const int32_t R = static_cast<int32_t>(n_slots);
+  const bool fp8 = fp8_act(dims);
+  const int x_terms = x_terms_of(fp8);
+  TileDesc* tiles = at<TileDesc>(ws, L.tiles);
+  int32_t* n_tiles = at<int32_t>(ws, L.n_tiles);
+  uint8_t* xs = at<uint8_t>(ws, L.xs);
+  float* xs_inv = at<float>(ws, L.xs_inv);
+  Tracer tr{nullptr, s};
+  // tile list first (the GEMMs read it without waiting), then the received rows in expert order
+  MOE_CHECK_CUDA(launch_build_tiles(local_offsets, dims->num_experts, tile_tokens(R, dims->num_experts), tiles,
+                                    n_tiles, s));
+  MOE_CHECK_CUDA(launch_gather_rows(static_cast<const uint16_t*>(recv_rows), row_pos, R, 1, dims->d, xs,
+                                    rows_layout(R, dims->num_experts, dims->d, x_terms, fp8), xs_inv, s));
+  // outputs unweighted (weight 1) to their received slot: out_rows[pos_row[sorted row]]
+  return run_gemms(true, fp8, w, dims->d, dims->d_ff, dims->num_experts, R, x_terms, xs, xs_inv, at<uint8_t>(ws, L.h),
+                   at<float>(ws, L.h_inv), tiles, n_tiles, pos_row, nullptr, out_rows, at<uint32_t>(ws, L.err), s, tr,
+                   "ep_gateup", "ep_down");
+}
+
+moe_status moe_ep_combine(const moe_dims* dims, int64_t n, const void* back_rows, const int32_t* tok_slot,
+                          int64_t n_slots, const float* topk_weight, void* out, int32_t out_is_fp32, cudaStream_t s) {
+  if (!dims || n < 0 || n_slots < 0) return MOE_ERR_INVALID_ARG;
+  if (!dims_ok(dims) || n * dims->top_k >= (int64_t(1) << 31) || n_slots >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (n == 0) return MOE_OK;
+  if (!back_rows || !tok_slot || !topk_weight || !out || !aligned(back_rows, 16) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (launch_ep_combine(static_cast<const uint16_t*>(back_rows), tok_slot, topk_weight, static_cast<int32_t>(n),
+                        dims->top_k, dims->d, n_slots, out, out_is_fp32, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status moe_check_bounded_wait(void* ws, cudaStream_t s) {

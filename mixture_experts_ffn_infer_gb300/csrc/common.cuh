@@ -154,14 +154,28 @@ cudaError_t launch_pack_tiles(const uint8_t* src0, const uint8_t* src1, uint8_t*
 cudaError_t launch_combine(const uint16_t* rows_f16, const uint16_t* shared_f16, const uint16_t* resid_bf16,
                            int32_t n, int32_t k, int32_t d, void* out, int32_t out_fp32, cudaStream_t s);
 
+// ep.cu (expert parallelism: the steps on either side of the exchanges)
+cudaError_t launch_ep_send_plan(const int32_t* ids, int32_t R, int32_t E, int32_t ep, const int32_t* offsets,
+                                const int32_t* inv_pos, int64_t capacity, int32_t* send_counts, int32_t* tok_slot,
+                                uint32_t* err, cudaStream_t s);
+cudaError_t launch_ep_gather(const uint16_t* x, const int32_t* tok_slot, int32_t n, int32_t k, int32_t d,
+                             int64_t n_slots, uint16_t* send, cudaStream_t s);
+int64_t ep_regroup_scratch_ints(int32_t epr, int32_t ep);
+cudaError_t launch_ep_regroup(const int32_t* cnt, int32_t epr, int32_t ep, int64_t capacity, int64_t n_slots,
+                              int32_t* local_counts, int32_t* local_offsets, int32_t* row_pos, int32_t* pos_row,
+                              int32_t* scratch, uint32_t* err, cudaStream_t s);
+cudaError_t launch_ep_combine(const uint16_t* back, const int32_t* tok_slot, const float* topk_weight, int32_t n,
+                              int32_t k, int32_t d, int64_t n_slots, void* out, int32_t out_fp32, cudaStream_t s);
+
 // moe_gemm.cu
 struct GemmLaunch {
   // weights: 3-D maps over [E][rows][K] e4m3, box 128 x 128 x 1, 128-byte swizzle
   const CUtensorMap* w0;        // gate (gate/up pass) or down (down pass)
   const CUtensorMap* w1;        // up (gate/up pass only)
   const CUtensorMap* act;       // 16-token tiles: 3-D map over [rows][3][K] e4m3, box 128 x terms x 16
+  const CUtensorMap* act_box_rows[3];  // wide tiles, exact scheme: boxes of 32, 64 and 96 token rows
   const CUtensorMap* act_box;   // wide tiles: f16 panels [K/64][rows][64], box 64 x 128 rows x 2 panels
-                                //   (exact scheme), or
+                                //   (exact scheme; act_box_rows[i] the same with boxes of 32 (i + 1) rows), or
                                 //   3-D map over [terms][rows][K], box 128 x 128 rows x terms (FP8)
   int32_t ntok;                 // token tile width (kNTokSmall or kNTokWide)
   int32_t terms;                // live activation terms per row (1 to 3)

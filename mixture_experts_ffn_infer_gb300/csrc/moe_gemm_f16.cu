@@ -42,7 +42,8 @@
 // list; warpgroups 0 and 1 hand registers to the epilogue warpgroups):
 //   0      weight producer: one 32 KB copy per K block (both tiles)
 //   1      MMA issuer (one thread)
-//   2      token producer: one TMA box [2 panels][128 rows][64 f16] per K block
+//   2      token producer: one TMA box [2 panels][rows][64 f16] per K block, the
+//          tile's rows rounded up to 32
 //   3      idle
 //   4..7   converters: warp 4 + q owns tensor-memory lanes 32q..32q+31, i.e.
 //          weight row 32q + lane of both blocks
@@ -146,6 +147,11 @@ __device__ __forceinline__ UnitF unit_f(const F16Args& a, int u, int upt) {
   x.has1 = x.nb1 < a.n_nb;
   return x;
 }
+
+// Rows of the token box that brings a tile of nv rows: nv rounded up to 32 (the
+// maps hold boxes of 32, 64, 96 and 128 rows).  The box's second panel starts
+// right after its rows, at rows * 128 bytes (a multiple of 4 KB).
+__device__ __forceinline__ int box_rows_of(int nv) { return min(kTokMax, (max(nv, 1) + 31) & ~31); }
 
 __device__ __forceinline__ void wait_drain_f(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -314,7 +320,9 @@ __device__ __forceinline__ void regs_inc_epi() {
 template <bool GATEUP, int WST, int TST>
 __global__ void __launch_bounds__(kThreadsF, 1)
 moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
-                    const __grid_constant__ CUtensorMap tm_tok, const F16Args a) {
+                    const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_tok32,
+                    const __grid_constant__ CUtensorMap tm_tok64, const __grid_constant__ CUtensorMap tm_tok96,
+                    const F16Args a) {
   using C = F16Cfg<WST, TST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -358,6 +366,9 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
       prefetch_tmap(&tm_w1);
     }
     prefetch_tmap(&tm_tok);
+    prefetch_tmap(&tm_tok32);
+    prefetch_tmap(&tm_tok64);
+    prefetch_tmap(&tm_tok96);
   }
   if (warp == kWarpMmaF) {
     tmem_alloc(smem_u32(tmem_slot), kTmemColsF);
@@ -434,7 +445,10 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
       uint32_t ti = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int row0 = unit_f(a, u, upt).row0;
+        const UnitF un = unit_f(a, u, upt);
+        // the tile's rows rounded up to 32: the box that brings them (panel 1 follows its rows)
+        const int rb = box_rows_of(un.nv);
+        const CUtensorMap* tm = rb == 32 ? &tm_tok32 : rb == 64 ? &tm_tok64 : rb == 96 ? &tm_tok96 : &tm_tok;
         for (int kb = 0; kb < num_kb; ++kb) {
           const int st = ti % TST;
           if (!wait_bounded(empty_t(st), ((ti / TST) & 1) ^ 1, abort_flag, a.err)) {
@@ -442,8 +456,8 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
             break;
           }
           const uint32_t dst = sbase + C::kTOff + st * kTStage;
-          mbar_arrive_expect_tx(full_t(st), kTStage);
-          tma_load_3d(dst, &tm_tok, full_t(st), 0, row0, 2 * kb, pol_t);  // panels 2 kb and 2 kb + 1
+          mbar_arrive_expect_tx(full_t(st), rb * 256);
+          tma_load_3d(dst, tm, full_t(st), 0, un.row0, 2 * kb, pol_t);  // panels 2 kb and 2 kb + 1
           ++ti;
         }
       }
@@ -470,7 +484,7 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
           }
           tc_fence_after();
           const uint32_t tb = sbase + C::kTOff + st * kTStage;
-          const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + kTPanel);
+          const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + box_rows_of(un.nv) * 128);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             if (m == 1 && !un.has1) break;
@@ -570,7 +584,7 @@ cudaError_t launch_f16(const GemmLaunch& g, cudaStream_t s) {
   auto kern = moe_gemm_f16_kernel<GATEUP, WST, TST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  if (!g.act_box) return cudaErrorInvalidValue;
+  if (!g.act_box || !g.act_box_rows[0] || !g.act_box_rows[1] || !g.act_box_rows[2]) return cudaErrorInvalidValue;
   // The register split waits until the pool covers it: launch only if it does.
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kern);
@@ -598,7 +612,7 @@ cudaError_t launch_f16(const GemmLaunch& g, cudaStream_t s) {
   // gate/up behind the row gather, down behind gate/up: dependent launches that stream
   // weights while their predecessor drains (both wait for its rows before reading them)
   return launch_maybe_overlapped(kern, g.num_sms, kThreadsF, C::kSmem, s, GATEUP ? g.overlap : true, *g.w0, *g.w1,
-                                 *g.act_box, a);
+                                 *g.act_box, *g.act_box_rows[0], *g.act_box_rows[1], *g.act_box_rows[2], a);
 }
 
 }  // namespace
