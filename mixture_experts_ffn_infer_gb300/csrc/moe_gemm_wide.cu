@@ -1,30 +1,28 @@
 // Grouped GEMMs of the routed experts for batches with more than a few rows
-// per expert.
+// per expert, under dynamic FP8 activations.
 //
 // "SwiGLU output" page, MLP class: expert(x) = down(silu(gate x) * up x);
 // "Mixture of experts" page, moe_infer: each expert runs on its contiguous
 // slice of sorted rows, outputs return to their positions weighted by
 // topk_weight; "Input features" page, quantisation config: e4m3 weights with
-// one fp32 scale per 128 x 128 block.
+// one fp32 scale per 128 x 128 block, activation_scheme "dynamic" (e4m3
+// activations with one scale amax / 448 per 128 features).
 //
-// The arithmetic is that of the 16-token kernel (moe_gemm.cu): e4m3 weights
-// straight into tcgen05.mma kind::f8f6f4, activations in the split format
-// (split3.cuh), the exact block-scaled product accumulated in fp32.  The
-// arrangement is for tiles of up to 128 tokens:
+// Weights and activations are both e4m3 codes, straight into tcgen05.mma
+// kind::f8f6f4; each K block (128) of the product gets its own fp32 partial,
+// multiplied by the weight block's scale and the activation group's scale in
+// the epilogue.  The arrangement is for tiles of up to 128 tokens:
 //
 //  * Tokens are the MMA's M side (128 rows = the 128 tensor-memory lanes) and
 //    two 128-row weight blocks its N side (N = 256): gate and up of the same
 //    output features (gate/up pass) or two consecutive row blocks of down
 //    (down pass).  The two 16 KB weight tiles of a K block sit back to back in
 //    shared memory and form one 256-row operand.
-//  * The activation terms are stacked along K: each term plane of a K block is
-//    a separate A operand and the MMAs of all terms accumulate into the same
-//    tensor-memory columns, smallest term first.
 //  * Two partial buffers of 256 columns fill tensor memory's 512 columns.
 //  * An epilogue thread owns one token (its tensor-memory lane) and 64 output
 //    features of each weight block.  Per K block it adds
-//    s_weight * 2^-s_act * partial to fp32 registers; at the end of a unit it
-//    writes its token's features with 16-byte stores.
+//    s_weight * s_act * partial to fp32 registers; at the end of a unit it
+//    writes its token's features with 32-byte stores.
 //
 // Warps (384 threads = 3 warpgroups, one CTA per SM, persistent over the unit
 // list; warpgroup 0 hands registers to the epilogue warpgroups):
@@ -32,21 +30,18 @@
 //          of the tiled layout, or 3-D TMA of the row-major layout), and an L2
 //          prefetch ahead when several token tiles share an expert's weights
 //   1      MMA issuer (one thread)
-//   2      activation producer: one 3-D TMA box [terms][128 rows][128 bytes]
-//          per K block
+//   2      activation producer: one TMA box [128 rows][128 bytes] per K block
 //   3      idle
 //   4..11  epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (the
 //          tile's tokens) and features 64 ((w - 4) / 4) .. +63 of each block
 //
-// At the end of a unit the gate/up epilogue forms h = silu(g) * u and writes
-// it as three term planes, one exponent per (token, 128 features) from the
-// maximum over both feature halves (their float exponents, exchanged as
-// bytes); the down epilogue writes f16(topk_weight * o) to the row's flat
-// position.  With dynamic FP8 activations (TX = 1: one term per value) the
-// gate/up epilogue exchanges the halves' maxima as floats and writes one plane
-// of codes of h / s, s = amax / 448.  Every wait is bounded; a wait that gives
-// up raises the abort flag and the device error word, and every role drains
-// what it has in flight before the kernel returns.
+// At the end of a unit the gate/up epilogue forms h = silu(g) * u, takes each
+// token's maximum over the 128 features of the unit (its 64 and the other
+// half's, exchanged as floats through shared memory and an eight-arrival
+// mbarrier) and writes the codes of h / s, s = amax / 448; the down epilogue
+// writes f16(topk_weight * o) to the row's flat position.  Every wait is
+// bounded; a wait that gives up raises the abort flag and the device error
+// word, and every role drains what it has in flight before the kernel returns.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -65,14 +60,14 @@ constexpr int kHalfF = 64;   // output features of each block per epilogue threa
 constexpr uint32_t kTmemColsW = 512;
 constexpr int kWTileBytes = 128 * 128;
 
-template <int TX, int WST, int AST>
+template <int WST, int AST>
 struct WideCfg {
   static constexpr int kWStage = 2 * kWTileBytes;          // both weight blocks of one K block
-  static constexpr int kAStage = TX * kTileMax * 128;      // the activation box: terms x 128 rows
+  static constexpr int kAStage = kTileMax * 128;           // the activation box: 128 rows of codes
   static constexpr int kAOff = WST * kWStage;
-  // h block maxima [parity][half][128 tokens]: float exponents as bytes, or (TX = 1) the floats
+  // h block maxima [parity][half][128 tokens]
   static constexpr int kRedOff = kAOff + AST * kAStage;
-  static constexpr int kRedBytes = 2 * 2 * kTileMax * (TX == 1 ? 4 : 1);
+  static constexpr int kRedBytes = 2 * 2 * kTileMax * 4;
   static constexpr int kBarOff = kRedOff + kRedBytes;
   static constexpr int kNumBars = 2 * WST + 2 * AST + 2 * 2 + 2 + 1;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
@@ -95,7 +90,6 @@ struct WideArgs {
   int32_t act_rows;
   void* out;                // gate/up: h term planes [3][act_rows][n_nb*128]; down: rows [.][n_nb*128] f16
   float* out_inv;           // gate/up: [n_nb][act_rows]
-  int64_t out_plane;        // gate/up: bytes between h term planes
   const int32_t* sorted_pos;
   const float* topk_weight;
   uint32_t* err;
@@ -171,25 +165,11 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&p)[64]) {
 // below 1e-36).
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// 16 values of one token, scaled by f1 * f2 = 2^s -> 16 codes of each term.
-__device__ __forceinline__ void split16(const float* v, float f1, float f2, uint32_t (&w1)[4], uint32_t (&w2)[4],
-                                        uint32_t (&w3)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t a1, a2, a3, b1, b2, b3;
-    split3_pair(make_float2(v[4 * i] * f1 * f2, v[4 * i + 1] * f1 * f2), a1, a2, a3);
-    split3_pair(make_float2(v[4 * i + 2] * f1 * f2, v[4 * i + 3] * f1 * f2), b1, b2, b3);
-    w1[i] = a1 | (b1 << 16);
-    w2[i] = a2 | (b2 << 16);
-    w3[i] = a3 | (b3 << 16);
-  }
-}
-
-template <bool GATEUP, int TX, int WST, int AST>
+template <bool GATEUP, int WST, int AST>
 __global__ void __launch_bounds__(kThreadsW, 1)
 moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                      const __grid_constant__ CUtensorMap tm_act, const WideArgs a) {
-  using C = WideCfg<TX, WST, AST>;
+  using C = WideCfg<WST, AST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -344,12 +324,8 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           const uint64_t adesc = desc_kmajor_sw128(sbase + C::kAOff + sa * C::kAStage);
           const uint32_t d = tmem + static_cast<uint32_t>(sd) * 256;
 #pragma unroll
-          for (int t = TX - 1; t >= 0; --t) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8(d, desc_advance(adesc, t * (kTileMax * 128) + kk * 32), desc_advance(wdesc, kk * 32), idesc,
-                     (t < TX - 1 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8(d, desc_advance(adesc, kk * 32), desc_advance(wdesc, kk * 32), idesc, kk > 0 ? 1u : 0u);
           tc_commit(empty_w(sw));
           tc_commit(empty_a(sa));
           tc_commit(dfull(sd));
@@ -430,7 +406,7 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
       if (!ok) break;
       bool overflow = false;
       if (GATEUP) {
-        // h = silu(g) * u; one exponent per (token, 128 features): the maximum of
+        // h = silu(g) * u; one scale per (token, 128 features) from the maximum of
         // this thread's 64 features and the other half's, exchanged through
         // red[ui & 1] and an eight-arrival mbarrier.
         float m = 0.f;
@@ -443,61 +419,29 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
         overflow &= valid;
         const int64_t ld = static_cast<int64_t>(n_nb) * 128;
         uint8_t* hp = static_cast<uint8_t*>(a.out) + row * ld + un.nb0 * 128 + hf * kHalfF;
-        if (TX == 1) {
-          // dynamic FP8: the scale needs the maximum itself, exchanged as a float
-          float* rf = reinterpret_cast<float*>(red) + (ui & 1) * 2 * kTileMax;
-          rf[hf * kTileMax + tok] = m;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(redbar(ui & 1));
-          ok = __all_sync(0xffffffffu, wait_bounded(redbar(ui & 1), (ui >> 1) & 1, abort_flag, a.err));
-          if (!ok) break;
-          if (valid) {
-            const float sc = fp8_block_scale(fmaxf(m, rf[(hf ^ 1) * kTileMax + tok]));
-#pragma unroll
-            for (int v = 0; v < kHalfF / 32; ++v) {
-              uint32_t t[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float* x4 = acc0 + 32 * v + 4 * i;
-                const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(x4[0], sc), __fdiv_rn(x4[1], sc)), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(x4[2], sc), __fdiv_rn(x4[3], sc)), __NV_SATFINITE, __NV_E4M3);
-                t[i] = lo | (hi << 16);
-              }
-              stg256(hp + 32 * v, t);
-            }
-            if (hf == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = sc;
-          }
-          if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(a.err, DEV_ERR_RANGE);
-          continue;
-        }
-        // the biased float exponent of the maximum is all the block scale needs
-        uint8_t* rb = red + (ui & 1) * 2 * kTileMax;
-        const uint32_t code = __float_as_uint(m) >> 23;  // m >= 0: 0 for zero or subnormal, 255 for inf
-        rb[hf * kTileMax + tok] = static_cast<uint8_t>(code);
+        float* rf = reinterpret_cast<float*>(red) + (ui & 1) * 2 * kTileMax;
+        rf[hf * kTileMax + tok] = m;
         __syncwarp();
         if (lane == 0) mbar_arrive(redbar(ui & 1));
         ok = __all_sync(0xffffffffu, wait_bounded(redbar(ui & 1), (ui >> 1) & 1, abort_flag, a.err));
         if (!ok) break;
         if (valid) {
-          // s = 8 - frexp exponent of the larger maximum (split_exponent), from the codes
-          const uint32_t c = max(code, static_cast<uint32_t>(rb[(hf ^ 1) * kTileMax + tok]));
-          const int sexp = (c == 0u || c == 255u) ? 0 : 134 - static_cast<int>(c);
-          const float f1 = pow2i(sexp >> 1), f2 = pow2i(sexp - (sexp >> 1));  // both factors stay normal
+          const float sc = fp8_block_scale(fmaxf(m, rf[(hf ^ 1) * kTileMax + tok]));
 #pragma unroll
           for (int v = 0; v < kHalfF / 32; ++v) {
-            uint32_t t1[8], t2[8], t3[8];
-            split16(acc0 + 32 * v, f1, f2, *reinterpret_cast<uint32_t(*)[4]>(&t1[0]),
-                    *reinterpret_cast<uint32_t(*)[4]>(&t2[0]), *reinterpret_cast<uint32_t(*)[4]>(&t3[0]));
-            split16(acc0 + 32 * v + 16, f1, f2, *reinterpret_cast<uint32_t(*)[4]>(&t1[4]),
-                    *reinterpret_cast<uint32_t(*)[4]>(&t2[4]), *reinterpret_cast<uint32_t(*)[4]>(&t3[4]));
-            stg256(hp + 32 * v, t1);
-            stg256(hp + a.out_plane + 32 * v, t2);
-            stg256(hp + 2 * a.out_plane + 32 * v, t3);
+            uint32_t t[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float* x4 = acc0 + 32 * v + 4 * i;
+              const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(x4[0], sc), __fdiv_rn(x4[1], sc)), __NV_SATFINITE, __NV_E4M3);
+              const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                  make_float2(__fdiv_rn(x4[2], sc), __fdiv_rn(x4[3], sc)), __NV_SATFINITE, __NV_E4M3);
+              t[i] = lo | (hi << 16);
+            }
+            stg256(hp + 32 * v, t);
           }
-          if (hf == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = pow2i(-(sexp >> 1)) *
-                                                                                      pow2i((sexp >> 1) - sexp);
+          if (hf == 0) a.out_inv[static_cast<int64_t>(un.nb0) * a.act_rows + row] = sc;
         }
       } else if (valid) {
         uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(dst) * n_nb * 128 + hf * kHalfF;
@@ -529,10 +473,10 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
   }
 }
 
-template <bool GATEUP, int TX, int WST, int AST>
+template <bool GATEUP, int WST, int AST>
 cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
-  using C = WideCfg<TX, WST, AST>;
-  auto kern = moe_gemm_wide_kernel<GATEUP, TX, WST, AST>;
+  using C = WideCfg<WST, AST>;
+  auto kern = moe_gemm_wide_kernel<GATEUP, WST, AST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   if (!g.act_box) return cudaErrorInvalidValue;
@@ -555,7 +499,6 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
   a.act_rows = g.act_rows;
   a.out = g.out;
   a.out_inv = g.out_inv;
-  a.out_plane = static_cast<int64_t>(g.act_rows) * g.n_nb * 128;
   a.sorted_pos = g.sorted_pos;
   a.topk_weight = g.topk_weight;
   a.err = g.err;
@@ -569,11 +512,11 @@ cudaError_t launch_wide(const GemmLaunch& g, cudaStream_t s) {
 // Stages (dynamic FP8, one term): four 32 KB weight stages (both blocks of one
 // K block) and four 16 KB activation stages; about 195 KB of shared memory.
 cudaError_t launch_gateup_wide(const GemmLaunch& g, cudaStream_t s) {
-  if (g.terms == 1 && g.fp8) return launch_wide<true, 1, 4, 4>(g, s);
+  if (g.terms == 1 && g.fp8) return launch_wide<true, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_down_wide(const GemmLaunch& g, cudaStream_t s) {
-  if (g.terms == 1 && g.fp8) return launch_wide<false, 1, 4, 4>(g, s);
+  if (g.terms == 1 && g.fp8) return launch_wide<false, 4, 4>(g, s);
   return cudaErrorInvalidValue;
 }
 
