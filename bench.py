@@ -60,25 +60,32 @@ def _bf16_peak(sustained):
     return (1700.0 if sustained else 1900.0), "fallback"
 
 
-# dense e4m3 / bf16 tensor throughput of the part (4.5 / 2.25 PFLOP/s nominal)
+# dense e4m3 / bf16 tensor throughput of the part (4.5 / 2.25 PFLOP/s nominal); f16 runs at the bf16 rate
 FP8_PER_BF16 = 2.0
 
-# what the tensor cores compute in, per activation scheme
-DTYPE_EXACT = "e4m3 weights x e4m3 split-term activations (exact scheme), fp32 accumulation"
+# what the tensor cores compute in, per activation scheme and tile width
+DTYPE_EXACT = "e4m3 weights x e4m3 split-term activations (exact scheme, 16-token tiles), fp32 accumulation"
+DTYPE_EXACT_WIDE = ("f16 x f16: e4m3 weights widened on chip with their block scale folded in, f16 activations "
+                    "with a power-of-two factor per row (exact scheme, 128-token tiles), fp32 accumulation")
 DTYPE_FP8 = "e4m3 weights x e4m3 dynamic activations (amax/448 per 128), fp32 accumulation"
 
 
-def kernel_roofline(kernel, alg_bytes, alg_flops, ms, hbm_gbs, hbm_src, e4m3_tflops, tensor_src, traffic):
+def wide_tiles(n_tokens, top_k, num_experts):
+    """The library's tile width rule: 128-token tiles once the batch averages 24 or more rows per expert."""
+    return n_tokens * top_k >= 24 * num_experts
+
+
+def kernel_roofline(kernel, alg_bytes, alg_flops, ms, hbm_gbs, hbm_src, tensor_tflops, tensor_src, traffic):
     """A kernel's algorithmic work against the roof that bounds it: HBM when its bytes take longer at the
-    copy bandwidth than its flops at the e4m3 tensor peak (the operand type of its MMAs), else the tensor
-    cores.  `achieved` is algorithmic bytes (or flops) over the measured duration."""
+    copy bandwidth than its flops at the tensor peak of its MMAs' operand type, else the tensor cores.
+    `achieved` is algorithmic bytes (or flops) over the measured duration."""
     t_hbm = alg_bytes / (hbm_gbs * 1e9)
-    t_tensor = alg_flops / (e4m3_tflops * 1e12)
+    t_tensor = alg_flops / (tensor_tflops * 1e12)
     r = {"kernel": kernel, "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": alg_flops, "kernel_ms": ms,
          "traffic": traffic, "t_roof_ms": max(t_hbm, t_tensor) * 1e3}
     if t_tensor > t_hbm:
         achieved = alg_flops / (ms / 1e3) / 1e12 if ms else None
-        r.update(bound="tensor", achieved=achieved, peak=e4m3_tflops, unit="TFLOP/s", peak_source=tensor_src)
+        r.update(bound="tensor", achieved=achieved, peak=tensor_tflops, unit="TFLOP/s", peak_source=tensor_src)
     else:
         achieved = alg_bytes / (ms / 1e3) / 1e9 if ms else None
         r.update(bound="hbm", achieved=achieved, peak=hbm_gbs, unit="GB/s", peak_source=hbm_src)
@@ -385,9 +392,15 @@ def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
     dominant = "gateup_swiglu"
     step_roof_ms = alg["step_bytes"] / (hbm * 1e9) * 1e3
     bf16, bf16_src = _bf16_peak(sustained=True)
-    # kernels timed inside a long step: the sustained tensor peak
+    # kernels timed inside a long step: the sustained tensor peak of their MMAs' operand type
     e4m3_peak = bf16 * FP8_PER_BF16
-    tensor_src = (f"{bf16_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (nominal e4m3 / bf16 dense ratio)")
+    f16_mma = not fp8 and wide_tiles(n, wl.top_k, wl.num_experts)
+    if f16_mma:
+        tensor_peak, tensor_src = bf16, f"{bf16_src} bf16_tflops_sustained (f16 operands, the bf16 rate)"
+    else:
+        tensor_peak = e4m3_peak
+        tensor_src = (f"{bf16_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (e4m3 operands: nominal e4m3 / bf16 "
+                      "dense ratio)")
     hbm_label = hbm_src + " (MEASURED_PEAKS.json hbm_gbs)" if hbm_src == "measured" else hbm_src
     tflops = alg["step_flops"] / (ms_step / 1e3) / 1e12
     traffic = _traffic(wl_name, dominant, fp8)
@@ -402,7 +415,7 @@ def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": DTYPE_FP8 if fp8 else DTYPE_EXACT,
+        "dtype": DTYPE_FP8 if fp8 else (DTYPE_EXACT_WIDE if f16_mma else DTYPE_EXACT),
         "data": "synthetic",
         "config": {"workload": wl_name, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
                    "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
@@ -413,9 +426,9 @@ def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
                        alg["step_bytes"] / 1e9),
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "roofline": kernel_roofline(dominant, alg["gateup_bytes"], alg["gateup_flops"], kern_ms.get(dominant),
-                                    hbm, hbm_label, e4m3_peak, tensor_src, traffic),
+                                    hbm, hbm_label, tensor_peak, tensor_src, traffic),
         "down_roofline": kernel_roofline("down_scatter", alg["down_bytes"], alg["down_flops"],
-                                         kern_ms.get("down_scatter"), hbm, hbm_label, e4m3_peak, tensor_src,
+                                         kern_ms.get("down_scatter"), hbm, hbm_label, tensor_peak, tensor_src,
                                          _traffic(wl_name, "down_scatter", fp8)),
         "step_roofline": {"bytes": alg["step_bytes"], "flops": alg["step_flops"], "t_roof_ms_hbm": step_roof_ms,
                           "frac_hbm": step_roof_ms / ms_step, "tflops": tflops,
