@@ -100,7 +100,6 @@ struct F16Cfg {
   static constexpr int kBarOff = kBufOff + 8 * kStageBufBytes;
   static constexpr int kNumBars = 2 * WST + 2 * TST + 2 * kAStages + 2 + 1;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
-  static constexpr int kPrefetch = (128 * 1024) / kWStageF;  // L2 prefetch distance in K blocks
   static_assert(kTOff % 1024 == 0 && kTStage % 1024 == 0, "operand stages stay 1024-byte aligned");
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
@@ -114,7 +113,6 @@ struct F16Args {
   int32_t n_nb;             // 128-row blocks of the weight matrix
   int32_t num_kb;           // K / 128
   int32_t pair;             // 1: unit = row blocks 2j, 2j+1 of w0 (down); 0: row block j of w0 and w1
-  int32_t l2_prefetch;      // prefetch weights into L2 ahead of their copies
   const float* tok_scale;   // [act_rows] power of two the token's f16 row was divided by (NULL = 1)
   int32_t act_rows;         // rows of the token matrix (and of h)
   void* out;                // gate/up: h in panels [n_nb*2][act_rows][64] f16; down: rows [.][n_nb*128] f16
@@ -391,23 +389,6 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
   if (warp == kWarpW) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      int pf_u = blockIdx.x, pf_kb = 0;
-      UnitF pf{};
-      auto prefetch_one = [&]() {
-        if (!a.l2_prefetch || pf_u >= total_units) return;
-        if (pf_kb == 0) pf = unit_f(a, pf_u, upt);
-        if (a.w_tiled) {
-          bulk_prefetch_l2(a.w_tiled + unit_off(pf.e, pf.ru, pf_kb), kWStageF);
-        } else {
-          tma_prefetch_3d(&tm_w0, pf_kb * 128, pf.nb0 * 128, pf.e);
-          if (pf.has1) tma_prefetch_3d(&tm_w1, pf_kb * 128, pf.nb1 * 128, pf.e);
-        }
-        if (++pf_kb == num_kb) {
-          pf_kb = 0;
-          pf_u += gridDim.x;
-        }
-      };
-      for (int i = 0; i < C::kPrefetch; ++i) prefetch_one();
       uint32_t wi = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
@@ -428,7 +409,6 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
             if (un.has1) tma_load_3d(dst + kWTileF, &tm_w1, full_w(sw), kb * 128, un.nb1 * 128, un.e, pol_w);
           }
           ++wi;
-          prefetch_one();
         }
       }
       if (!ok)
@@ -599,10 +579,6 @@ cudaError_t launch_f16(const GemmLaunch& g, cudaStream_t s) {
   a.n_nb = g.n_nb;
   a.num_kb = g.num_kb;
   a.pair = GATEUP ? 0 : 1;
-  // No L2 prefetch ahead of the weight copies: each prefetch is one more bulk
-  // operation for the SM's copy engine, whose operation rate (not its bytes)
-  // bounds this kernel's K-block period.
-  a.l2_prefetch = 0;
   a.tok_scale = g.act_inv;
   a.act_rows = g.act_rows;
   a.out = g.out;
@@ -620,8 +596,13 @@ cudaError_t launch_f16(const GemmLaunch& g, cudaStream_t s) {
 // Stages: three 32 KB weight stages (both blocks of one K block; released as soon
 // as they are converted) and three 32 KB token stages (128 rows x 128 f16, one
 // TMA box each), plus 8 KB of epilogue transpose buffers; 201 KB of shared
-// memory.  Two copies per K block: an SM's copy engine completes about 3.5
-// million copies per second, so that rate and the MMAs are about even.
+// memory.  What bounds the K-block period (measured with timestamps and copy
+// probes): a stage is reissued only when its previous contents are consumed, and
+// while an SM streams weights from DRAM its token boxes (L2 hits, ~840 cycles
+// alone) take as long as the weight copies, ~3,700-4,200 cycles; with three
+// stages a side the period is about (that latency + the stage's hold time) / 3,
+// ~1,750 cycles against ~1,050 of MMA issue.  More stages do not fit; an L2
+// prefetch of the weights ahead of their copies did not shorten the period.
 cudaError_t launch_gateup_f16(const GemmLaunch& g, cudaStream_t s) { return launch_f16<true, 3, 3>(g, s); }
 cudaError_t launch_down_f16(const GemmLaunch& g, cudaStream_t s) { return launch_f16<false, 3, 3>(g, s); }
 
