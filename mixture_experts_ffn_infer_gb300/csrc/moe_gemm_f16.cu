@@ -123,6 +123,7 @@ struct F16Args {
 
 struct UnitF {
   int e, row0, nv, ru, nb0, nb1;
+  int reuse;  // tiles of the unit's chunk: units that read the same weights side by side
   bool has1;
 };
 
@@ -143,6 +144,7 @@ __device__ __forceinline__ UnitF unit_f(const F16Args& a, int u, int upt) {
   x.nb0 = a.pair ? 2 * j : j;
   x.nb1 = a.pair ? 2 * j + 1 : j;
   x.has1 = x.nb1 < a.n_nb;
+  x.reuse = n;
   return x;
 }
 
@@ -388,11 +390,14 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
   if (warp < kWarpConv) regs_dec_low();  // warpgroup 0: copies, MMA
   if (warp == kWarpW) {
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // weights read by one tile leave L2 first; weights that the chunk's other tiles
+      // read next to it stay at normal priority
+      const uint64_t pol_once = policy_evict_first(), pol_shared = policy_evict_normal();
       uint32_t wi = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const UnitF un = unit_f(a, u, upt);
+        const uint64_t pol_w = un.reuse > 1 ? pol_shared : pol_once;
         for (int kb = 0; kb < num_kb; ++kb) {
           const int sw = wi % WST;
           if (!wait_bounded(empty_w(sw), ((wi / WST) & 1) ^ 1, abort_flag, a.err)) {
