@@ -43,17 +43,30 @@
  *     n * k < 2^31.  Pointers handed to the tensor-memory-access engine
  *     (weights, x) must be 16-byte aligned; the workspace 256-byte aligned.
  *
- * Precision: the expert GEMMs multiply e4m3 operands on the tensor cores
- * into fp32 accumulators.  Under MOE_ACT_EXACT (the default; moe_dims
- * below also offers dynamic FP8 activations) each activation row is carried as a sum of e4m3
- * terms sharing one power-of-two scale per 128 columns: two terms hold a bf16
- * value exactly (x, and the bf16 RMSNorm output) unless it lies more than
- * 2^10 below its block's maximum (then within 2^-18 of that maximum), three
- * terms carry silu(g) * u (h, formed in fp32) to about 12 significant bits.  Each
- * 128 x 128 weight block scale and the activation scale multiply the fp32
- * partial sum of their block.  Each weighted expert row is stored as f16, the
- * k rows are summed in fp32 in ascending slot order and the result is rounded
- * once to bf16 (or kept in fp32 when out_is_fp32 is set).
+ * Precision: the expert GEMMs run on the tensor cores into fp32 accumulators.
+ * Under MOE_ACT_EXACT (the default; moe_dims below also offers dynamic FP8
+ * activations) the operands depend on the tile width the batch gets (16-token
+ * tiles while it averages fewer than 24 routed rows per expert, tiles of up to
+ * 128 tokens from there on):
+ *   16-token tiles: e4m3 weights x e4m3 activation terms.  Each activation row
+ *     is carried as a sum of e4m3 terms sharing one power-of-two scale per 128
+ *     columns: two terms hold a bf16 value exactly (x, and the bf16 RMSNorm
+ *     output) unless it lies more than 2^10 below its block's maximum (then
+ *     within 2^-18 of that maximum), three terms carry silu(g) * u (h, formed
+ *     in fp32) to about 12 significant bits.  Each 128 x 128 weight block scale
+ *     and the activation scale multiply the fp32 partial sum of their block.
+ *   wide tiles: f16 x f16.  Each e4m3 weight code is widened to f16 exactly and
+ *     multiplied by its block's scale times a power of two per weight row
+ *     block (one f16 rounding, at most 2^-11 relative, while the block's scales
+ *     along K lie within 2^10 of their largest); each activation row is the f16
+ *     of the bf16 row times a power of two of its own, exact for every value
+ *     within 2^28 of the row's largest magnitude; h is the f16 of
+ *     silu(g) * u (at most 2^-11 relative from 2^-14 up, below that within
+ *     2^-25 absolute).  The whole K extent accumulates in fp32 and the powers of
+ *     two are undone in the epilogue.
+ * Each weighted expert row is stored as f16, the k rows are summed in fp32 in
+ * ascending slot order and the result is rounded once to bf16 (or kept in fp32
+ * when out_is_fp32 is set).
  */
 #ifndef MOE_FFN_H
 #define MOE_FFN_H
@@ -79,13 +92,11 @@ typedef enum {
 
 /* Activation schemes ("Input features" page, quantisation config: fmt e4m3,
  * activation_scheme "dynamic", weight blocks of 128 x 128).
- *   MOE_ACT_EXACT        activations are never quantised: every row is
- *                        carried as e4m3 split terms (see Precision above),
- *                        exact for bf16 values within 2^10 of their block's
- *                        maximum (smaller ones within 2^-18 of it) and about
- *                        12 significant bits for h, so the result is the
- *                        function of the FP8 weights to within those
- *                        roundings and the f16 rows.
+ *   MOE_ACT_EXACT        activations are never quantised to e4m3: every row
+ *                        is carried as e4m3 split terms (16-token tiles) or
+ *                        as a scaled f16 row (wide tiles), see Precision
+ *                        above, so the result is the function of the FP8
+ *                        weights to within those roundings and the f16 rows.
  *   MOE_ACT_FP8_DYNAMIC  every row entering a linear (x, the normalised row,
  *                        h) is quantised on the fly per group of 128
  *                        features: scale s = amax / 448 in fp32 (1 for an

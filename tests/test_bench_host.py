@@ -2,8 +2,10 @@
 each GEMM and how the fraction is formed.
 
 A GEMM is HBM-bound when its algorithmic bytes take longer at the copy bandwidth
-than its algorithmic flops at the e4m3 tensor peak: the decode and prefill
-batches are, the full block (683 rows per expert) is not."""
+than its algorithmic flops at the tensor peak of its MMAs' operand type (e4m3
+for 16-token tiles and the dynamic FP8 scheme, f16 for the exact scheme's wide
+tiles): the decode and prefill batches are, the full block (683 rows per expert)
+is not."""
 
 import torch
 
@@ -79,3 +81,20 @@ def test_traffic_record_is_used_only_for_its_scheme_and_unchanged_source(tmp_pat
     (src / "k.cu").write_text("kernel v2\n")                    # the kernel changed since the capture
     assert bench._traffic("w", "gateup_swiglu") is None
     assert bench._traffic("w", "gateup_swiglu", fp8=True) is None
+
+
+def test_tile_width_rule_and_tensor_peak_per_workload():
+    # wide tiles from an average of 24 routed rows per expert on (the library's tile_tokens)
+    assert not bench.wide_tiles(24 * 384 // 8 - 1, 8, 384)
+    assert bench.wide_tiles(24 * 384 // 8, 8, 384)
+    widths = {name: bench.wide_tiles(wl.n_tokens, wl.top_k, wl.num_experts) for name, wl in syn.WORKLOADS.items()}
+    assert widths["k2_decode"] is False
+    assert widths["k2_prefill"] and widths["k2_skewed"] and widths["k2_block"]
+    # at the f16 rate the full block's GEMMs stay tensor-bound, prefill's HBM-bound
+    BF16 = 1720.0
+    _, a = _alg("k2_block", 384)
+    r = bench.kernel_roofline("gateup_swiglu", a["gateup_bytes"], a["gateup_flops"], 1.0, HBM, "m", BF16, "m", None)
+    assert r["bound"] == "tensor" and r["peak"] == BF16
+    _, a = _alg("k2_prefill", 384)
+    r = bench.kernel_roofline("gateup_swiglu", a["gateup_bytes"], a["gateup_flops"], 1.0, HBM, "m", BF16, "m", None)
+    assert r["bound"] == "hbm"
