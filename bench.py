@@ -239,6 +239,22 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+L2_BYTES = 129e6  # GB300 L2
+
+
+def run_config(wl, wl_name, n, fp8, alg, world):
+    """The workload a line measures; both arms report it alike."""
+    return {"workload": wl_name, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
+            "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
+            "full_block": wl.full_block, "weights": "e4m3, fp32 scale per 128x128 block, tiled layout",
+            "act_scheme": "fp8_dynamic" if fp8 else "exact",
+            "touched_experts": alg["touched_experts"],
+            "l2": ("inputs larger than L2: %.2f GB of touched expert weights per step" if alg["step_bytes"] > L2_BYTES
+                   else "inputs fit in L2 (%.3f GB per step): no flush between steps, a latency figure") % (
+                       alg["step_bytes"] / 1e9),
+            "parallelism": f"replicas{world}" if world > 1 else "single"}
+
+
 def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
     """One workload: W warm-up steps, K untimed-event steps timed as a whole (the headline), then a
     separate sample of steps with events around the GEMMs (per-kernel times), the host-buffer end-to-end
@@ -333,39 +349,45 @@ def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
 
     # end to end through the same C ABI with host buffers: every step copies its inputs from pinned
     # host memory and reads its result back, all inside the timed region.  As a serving loop would,
-    # the copies run on their own stream with two buffer sets, so step i + 1's upload and step i's
-    # download overlap step i's compute.
+    # uploads and downloads run on streams of their own with two buffer sets, so step i + 1's upload
+    # and step i - 1's download overlap step i's compute (and each other).
     xh, idh, wh = x.pin_memory(), ids.pin_memory(), w.pin_memory()
     oh = torch.empty(n, wl.d, dtype=torch.bfloat16).pin_memory()
     sets = [(torch.empty_like(xd), torch.empty_like(idsd), torch.empty_like(wd), torch.empty_like(out))
             for _ in range(2)]
-    copy_stream = torch.cuda.Stream(dev)
+    up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     uploaded = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
 
     def upload(b):
         xe, ide, we, _ = sets[b]
-        with torch.cuda.stream(copy_stream):
+        with torch.cuda.stream(up_stream):
             xe.copy_(xh, non_blocking=True)
             ide.copy_(idh, non_blocking=True)
             we.copy_(wh, non_blocking=True)
-            uploaded[b].record(copy_stream)
+            uploaded[b].record(up_stream)
 
     def e2e_run(steps):
-        copy_stream.wait_stream(stream)
+        up_stream.wait_stream(stream)
+        down_stream.wait_stream(stream)
         upload(0)
         for i in range(steps):
             b = i % 2
             stream.wait_event(uploaded[b])
+            if i >= 2:
+                stream.wait_event(downloaded[b])      # step i - 2's result has left this set
             step(None, *sets[b])
             computed[b].record(stream)
             if i + 1 < steps:
-                copy_stream.wait_event(computed[1 - b])   # step i - 1 is done with the other set
+                up_stream.wait_event(computed[1 - b])   # step i - 1 is done with the other set's inputs
                 upload(1 - b)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(computed[b])
+            down_stream.wait_event(computed[b])
+            with torch.cuda.stream(down_stream):
                 oh.copy_(sets[b][3], non_blocking=True)
-        stream.wait_stream(copy_stream)
+                downloaded[b].record(down_stream)
+        stream.wait_stream(up_stream)
+        stream.wait_stream(down_stream)
 
     e2e_ms = float("nan")
     if not args.no_e2e:
@@ -417,14 +439,7 @@ def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
         "vs_baseline": None,
         "dtype": DTYPE_FP8 if fp8 else (DTYPE_EXACT_WIDE if f16_mma else DTYPE_EXACT),
         "data": "synthetic",
-        "config": {"workload": wl_name, "n_tokens_per_gpu": n, "d": wl.d, "d_ff": wl.d_ff,
-                   "num_experts": wl.num_experts, "top_k": wl.top_k, "routing": wl.routing,
-                   "full_block": wl.full_block, "weights": "e4m3, fp32 scale per 128x128 block, tiled layout",
-                   "act_scheme": "fp8_dynamic" if fp8 else "exact",
-                   "touched_experts": alg["touched_experts"],
-                   "l2": "inputs larger than L2: %.2f GB of touched expert weights per step" % (
-                       alg["step_bytes"] / 1e9),
-                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "config": run_config(wl, wl_name, n, fp8, alg, world),
         "roofline": kernel_roofline(dominant, alg["gateup_bytes"], alg["gateup_flops"], kern_ms.get(dominant),
                                     hbm, hbm_label, tensor_peak, tensor_src, traffic),
         "down_roofline": kernel_roofline("down_scatter", alg["down_bytes"], alg["down_flops"],
@@ -439,8 +454,8 @@ def measure(args, wl, wl_name, bank, bank_t, rank, world, local_rank, dev):
         "e2e": None if args.no_e2e else {"value": tokens * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * 2 + ids.numel() * 4 + w.numel() * 4),
                 "d2h_bytes_per_step": int(n * wl.d * 2), "ms_per_step": e2e_ms / args.steps,
-                "copies": "pinned host buffers; uploads and downloads on a copy stream, overlapping the "
-                          "neighbouring steps' compute (two buffer sets)"},
+                "copies": "pinned host buffers; uploads and downloads on streams of their own, overlapping "
+                          "the neighbouring steps' compute and each other (two buffer sets)"},
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -543,9 +558,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "n_tokens_per_gpu": x.shape[0], "d": wl.d, "d_ff": wl.d_ff,
-                   "num_experts": wl.num_experts, "top_k": wl.top_k,
-                   "act_scheme": "fp8_dynamic" if args.act == "fp8" else "exact"},
+        "config": run_config(wl, args.workload, x.shape[0], args.act == "fp8", algorithmic(wl, [ids], x.shape[0]),
+                             int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{per_step} tokens of the {wl.name} batch per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
