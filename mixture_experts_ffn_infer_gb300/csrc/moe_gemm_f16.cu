@@ -41,7 +41,7 @@
 // Warps (512 threads = 4 warpgroups, one CTA per SM, persistent over the unit
 // list; warpgroups 0 and 1 hand registers to the epilogue warpgroups):
 //   0      weight producer: one 32 KB copy per K block (both tiles)
-//   1      MMA issuer (one thread)
+//   1      MMA issuer (the warp runs the loop, one elected thread issues)
 //   2      token producer: one TMA box [2 panels][rows][64 f16] per K block, the
 //          tile's rows rounded up to 32
 //   3      idle
@@ -451,25 +451,25 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
     }
     __syncwarp();
   } else if (warp == kWarpMmaF) {
-    if (lane == 0) {
-      uint32_t it = 0, ui = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
-        const UnitF un = unit_f(a, u, upt);
-        const int n_mma = (max(un.nv, 1) + 15) & ~15;  // N: the tile's rows, a multiple of 16
-        const uint32_t idesc = idesc_f16_f32(128, n_mma);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int st = it % TST, sa = it % kAStages;
-          // the first K block overwrites the accumulators: they must have been read out
-          if ((kb == 0 && !wait_bounded(dempty, (ui & 1) ^ 1, abort_flag, a.err)) ||
-              !wait_bounded(full_t(st), (it / TST) & 1, abort_flag, a.err) ||
-              !wait_bounded(afull(sa), (it / kAStages) & 1, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tb = sbase + C::kTOff + st * kTStage;
-          const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + box_rows_of(un.nv) * 128);
+    // The whole warp runs the loop (descriptors stay warp-uniform); one elected thread issues
+    // the MMAs and their commits.
+    uint32_t it = 0, ui = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
+      const UnitF un = unit_f(a, u, upt);
+      const int n_mma = (max(un.nv, 1) + 15) & ~15;  // N: the tile's rows, a multiple of 16
+      const uint32_t idesc = idesc_f16_f32(128, n_mma);
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int st = it % TST, sa = it % kAStages;
+        // the first K block overwrites the accumulators: they must have been read out
+        ok = __all_sync(0xffffffffu, (kb != 0 || wait_bounded(dempty, (ui & 1) ^ 1, abort_flag, a.err)) &&
+                                         wait_bounded(full_t(st), (it / TST) & 1, abort_flag, a.err) &&
+                                         wait_bounded(afull(sa), (it / kAStages) & 1, abort_flag, a.err));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tb = sbase + C::kTOff + st * kTStage;
+        const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + box_rows_of(un.nv) * 128);
+        if (elect_one()) {
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             if (m == 1 && !un.has1) break;
@@ -484,10 +484,12 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
           tc_commit(aempty(sa));
           if (kb == num_kb - 1) tc_commit(dfull);
         }
+        __syncwarp();
       }
-      tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
-      wait_drain_f(drain_bar, 0);
     }
+    if (elect_one()) tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
+    __syncwarp();
+    wait_drain_f(drain_bar, 0);
     __syncwarp();
   } else if (warp >= kWarpConv && warp < kWarpEpi) {
     // converters: weight row r of both blocks, K block by K block, into the A stages
