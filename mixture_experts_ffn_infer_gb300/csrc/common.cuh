@@ -53,6 +53,14 @@ struct TileDesc {
   int32_t chunk;
 };
 
+// Written beside a tile count (n_tiles[2], the count in n_tiles[0]): 1 when at
+// least 90 % of the tiles belong to experts cut into two or more tiles, whose
+// weights are then read by several tiles and mostly from L2 after the first;
+// the f16 GEMM then gives its token ring the deeper share of its stages.
+__host__ __device__ inline int32_t tiles_share_weights(int multi_tiles, int tiles) {
+  return tiles > 0 && 10LL * multi_tiles >= 9LL * tiles ? 1 : 0;
+}
+
 constexpr int kTileChunk = 8;
 __host__ __device__ inline int32_t tile_chunk_code(int idx_in_slice, int tiles_in_slice) {
   const int c = idx_in_slice / kTileChunk;
@@ -186,7 +194,7 @@ struct GemmLaunch {
   const float* s0;              // scales [E][n_nb][num_kb]
   const float* s1;
   const TileDesc* tiles;
-  const int32_t* n_tiles;
+  const int32_t* n_tiles;       // [0] tile count, [2] tiles_share_weights of the list
   int32_t n_nb;                 // weight-row blocks of 128 (output features / 128)
   // A unit is one token tile times two weight blocks: gate/up pass = row block j
   // of w0 and of w1; down pass = row blocks 2j and 2j + 1 of w0.

@@ -26,9 +26,9 @@
 //               into a ring.
 //   warp 2      activation producer: a 3-D box of NTOK rows x TT terms x 128 bytes
 //               into its own ring, so neither ring throttles the other.
-//   warp 1      MMA issuer (the warp runs the loop, one elected thread
-//               issues): 4 x tcgen05.mma (M=128, N=TT NTOK, K=32) per
-//               weight block into a fresh fp32 partial in tensor memory.
+//   warp 1      MMA issuer (one thread, elected): 4 x tcgen05.mma (M=128,
+//               N=TT NTOK, K=32) per weight block into a fresh fp32 partial
+//               in tensor memory.
 //   warps 4-7   epilogue: per token, sum its TT term columns, multiply by
 //               the weight block's fp32 scale and the activation block's factor
 //               (2^-s, or the FP8 scale) and add to fp32 accumulators in
@@ -319,29 +319,32 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
-    // The whole warp runs the loop (descriptors stay warp-uniform); one elected thread issues
-    // the MMAs and their commits.
-    constexpr uint32_t idesc = idesc_f16_f32(128, NB);  // kind::f8f6f4: E4M3 has format code 0, as f16
-    uint32_t it = 0, wt = 0;  // K blocks and weight stages consumed
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const bool has1 = unit16(a, u, upt, L).has1;
-      for (int kb0 = 0; ok && kb0 < num_kb; kb0 += KPS, ++wt) {
-        const int sw = wt % WST;
-        const int nk = min(KPS, num_kb - kb0);
-        ok = __all_sync(0xffffffffu, wait_bounded(full_w(sw), (wt / WST) & 1, abort_flag, a.err));
-        if (!ok) break;
-        const uint32_t wst = sbase + sw * C::kWStage;
-        const uint64_t wdesc = desc_kmajor_sw128(wst);
-        for (int j = 0; j < nk; ++j, ++it) {
-          const int sb = it % BST, sd = it % DST;
-          ok = __all_sync(0xffffffffu, wait_bounded(full_b(sb), (it / BST) & 1, abort_flag, a.err) &&
-                                           wait_bounded(dempty(sd), ((it / DST) & 1) ^ 1, abort_flag, a.err));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t bdesc = desc_kmajor_sw128(sbase + C::kBOffset + sb * C::kBStage);
-          const uint64_t wj = desc_advance(wdesc, j * C::kWKb);
-          if (elect_one()) {
+    // One elected thread runs the whole loop: its waits, MMAs and commits.
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_f16_f32(128, NB);  // kind::f8f6f4: E4M3 has format code 0, as f16
+      uint32_t it = 0, wt = 0;  // K blocks and weight stages consumed
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const bool has1 = unit16(a, u, upt, L).has1;
+        for (int kb0 = 0; ok && kb0 < num_kb; kb0 += KPS, ++wt) {
+          const int sw = wt % WST;
+          const int nk = min(KPS, num_kb - kb0);
+          if (!wait_bounded(full_w(sw), (wt / WST) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t wst = sbase + sw * C::kWStage;
+          const uint64_t wdesc = desc_kmajor_sw128(wst);
+          for (int j = 0; j < nk; ++j, ++it) {
+            const int sb = it % BST, sd = it % DST;
+            if (!wait_bounded(full_b(sb), (it / BST) & 1, abort_flag, a.err) ||
+                !wait_bounded(dempty(sd), ((it / DST) & 1) ^ 1, abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t bdesc = desc_kmajor_sw128(sbase + C::kBOffset + sb * C::kBStage);
+            const uint64_t wj = desc_advance(wdesc, j * C::kWKb);
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               if (m == 1 && !has1) break;
@@ -354,15 +357,12 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant
             tc_commit(empty_b(sb));
             tc_commit(dfull(sd));
           }
-          __syncwarp();
+          if (ok) tc_commit(empty_w(sw));  // the stage's weights are free once its MMAs complete
         }
-        if (ok && elect_one()) tc_commit(empty_w(sw));  // the stage's weights are free once its MMAs complete
-        __syncwarp();
       }
+      tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
+      wait_drain(drain_bar, 0);
     }
-    if (elect_one()) tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
-    __syncwarp();
-    wait_drain(drain_bar, 0);
     __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
     pdl_wait();  // activation exponents come from the previous kernel

@@ -41,7 +41,7 @@
 // Warps (512 threads = 4 warpgroups, one CTA per SM, persistent over the unit
 // list; warpgroups 0 and 1 hand registers to the epilogue warpgroups):
 //   0      weight producer: one 32 KB copy per K block (both tiles)
-//   1      MMA issuer (the warp runs the loop, one elected thread issues)
+//   1      MMA issuer (one thread, elected)
 //   2      token producer: one TMA box [2 panels][rows][64 f16] per K block, the
 //          tile's rows rounded up to 32
 //   3      idle
@@ -74,7 +74,6 @@ constexpr int kWTileF = 128 * 128;             // e4m3 bytes of one 128 x 128 we
 constexpr int kWStageF = 2 * kWTileF;          // both weight blocks of one K block
 constexpr int kTPanel = kTokMax * 128;         // one 64-column panel of 128 token rows (f16)
 constexpr int kTStage = 2 * kTPanel;           // a K block of 128 tokens: two panels, one TMA box
-constexpr int kStageBufBytes = 2 * 8 * 32 * 2;   // per epilogue warp: 2 blocks x 8 tokens x 32 features of f16
 constexpr uint32_t kTmemColsF = 512;
 constexpr uint32_t kAccCols = 128;             // accumulator columns per weight block
 constexpr uint32_t kAOff = 256;                // first A stage column
@@ -93,16 +92,30 @@ constexpr int kRegsEpi = 176;
 constexpr int kRegsAtLaunch = 128;  // 65536 / 512
 static_assert(128 * kRegsLow + 128 * kRegsConv + 256 * kRegsEpi <= kThreadsF * kRegsAtLaunch, "register split");
 
-template <int WST, int TST>
+// Seven 32 KB operand stages, split between the weight ring and the token ring
+// at run time: 3 + 4 when weights stream from DRAM, 2 + 5 when nearly every
+// tile's weights are shared with the expert's other tiles (they come from L2
+// after the first tile, and the token stream needs the deeper ring).
 struct F16Cfg {
-  static constexpr int kTOff = WST * kWStageF;
-  static constexpr int kBufOff = kTOff + TST * kTStage;          // epilogue buffers, 8 warps
-  static constexpr int kBarOff = kBufOff + 8 * kStageBufBytes;
-  static constexpr int kNumBars = 2 * WST + 2 * TST + 2 * kAStages + 2 + 1;
+  static constexpr int kStages = 7;
+  static constexpr int kWMax = 3;   // weight stages at most
+  static constexpr int kTMax = 5;   // token stages at most
+  static constexpr int kBarOff = kStages * kWStageF;
+  // full / empty of each ring at its largest, A stages, accumulators full / empty, drain
+  static constexpr int kNumBars = 2 * kWMax + 2 * kTMax + 2 * kAStages + 2 + 1;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8 + 16;
-  static_assert(kTOff % 1024 == 0 && kTStage % 1024 == 0, "operand stages stay 1024-byte aligned");
+  static_assert(kWStageF == kTStage && kTStage % 1024 == 0, "operand stages stay 1024-byte aligned");
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
+
+// Stage and phase parity of the i-th use of a ring of A (is_a) or B stages;
+// both sizes are compile-time constants, so no division at run time.
+template <int A, int B>
+__device__ __forceinline__ int ring_stage(uint32_t i, bool is_a, uint32_t& parity) {
+  const uint32_t q = is_a ? i / A : i / B;
+  parity = q & 1u;
+  return static_cast<int>(i - q * (is_a ? A : B));
+}
 
 struct F16Args {
   const uint8_t* w_tiled;   // non-null: tiled layout (both blocks of a K block in 32 KB), bulk copies
@@ -211,14 +224,14 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + _
 
 // End of a unit for one epilogue warp (lanes 32q.. = output features 32q..,
 // tokens 64 half .. + 63): read the warp's 64 columns of both accumulators
-// with one wait and release them; then, 8 tokens at a time, form the outputs
-// into the warp's transpose buffer (buf[block][token][32 features] of f16) and
-// write each token's 32 features with 16-byte stores.
+// with one wait and release them; then, token by token, form the outputs and
+// write them straight from registers: the 32 lanes hold 32 consecutive
+// features of the token, one 64-byte store per token and weight block.
 template <bool GATEUP>
 __device__ __forceinline__ bool unit_epilogue(const F16Args& a, const UnitF un, const int cw0, const int cw1,
                                               const uint32_t ui, const uint32_t tmem, const int q, const int half,
                                               const uint32_t dfull, const uint32_t dempty,
-                                              volatile uint32_t* abort_flag, uint8_t* buf) {
+                                              volatile uint32_t* abort_flag) {
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
   const float f0 = ldexpf(1.0f, -cw0), f1 = ldexpf(1.0f, -cw1);
@@ -259,49 +272,31 @@ __device__ __forceinline__ bool unit_epilogue(const F16Args& a, const UnitF un, 
   __syncwarp();
   if (lane == 0) mbar_arrive(dempty);
   bool overflow = false;
-  uint16_t* bw = reinterpret_cast<uint16_t*>(buf);
-  const int ti = lane >> 2, seg = lane & 3;   // store phase: token ti of the group, features 8 seg..
-  const int f = q * 32 + 8 * seg;            // that feature within the 128-row block
+  const int f = q * 32 + lane;  // this lane's feature within the 128-row block
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    if (8 * g >= nt) break;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int jj = 8 * g + i;
-      const float tfj = __shfl_sync(0xffffffffu, tf[g >> 2], jj & 31);
-      float v0, v1 = 0.f;
-      if (GATEUP) {
-        const float gg = __uint_as_float(p0[jj]) * (f0 * tfj), uu = __uint_as_float(p1[jj]) * (f1 * tfj);
-        v0 = silu_f(gg) * uu;
-      } else {
-        v0 = __uint_as_float(p0[jj]) * (f0 * tfj);
-        if (has1) v1 = __uint_as_float(p1[jj]) * (f1 * tfj);
-      }
-      if (jj < nt) overflow |= !(fabsf(v0) < 65520.f) || !(fabsf(v1) < 65520.f);  // f16 rounds these to inf
-      bw[i * 32 + lane] = __half_as_ushort(__float2half_rn(v0));
-      if (!GATEUP) bw[256 + i * 32 + lane] = __half_as_ushort(__float2half_rn(v1));
-    }
-    __syncwarp();
-    const int t = 8 * g + ti;  // this lane's token within the warp's 64
-    const int dst = __shfl_sync(0xffffffffu, dstv[g >> 2], t & 31);  // token t is in half g / 4
-#pragma unroll
-    for (int m = 0; m < (GATEUP ? 1 : 2); ++m) {
-      if (m == 1 && !has1) break;
-      const uint4 o = reinterpret_cast<const uint4*>(buf + m * 512)[lane];  // token ti, features 8 seg..
-      if (t < nt) {
-        if (GATEUP) {
-          // h panels of 64 features: panel 2 nb0 + f / 64, row dst (the sorted row)
-          const int64_t panel = 2 * un.nb0 + (f >> 6);
-          *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + panel * a.act_rows * 128 +
-                                    static_cast<int64_t>(dst) * 128 + (f & 63) * 2) = o;
-        } else {
-          const int nb = m == 0 ? un.nb0 : un.nb1;
-          *reinterpret_cast<uint4*>(static_cast<__half*>(a.out) + static_cast<int64_t>(dst) * a.n_nb * 128 +
-                                    nb * 128 + f) = o;
-        }
+  for (int jj = 0; jj < 64; ++jj) {
+    if (jj >= nt) break;
+    const float tfj = __shfl_sync(0xffffffffu, tf[jj >> 5], jj & 31);
+    const int dst = __shfl_sync(0xffffffffu, dstv[jj >> 5], jj & 31);
+    if (GATEUP) {
+      const float gg = __uint_as_float(p0[jj]) * (f0 * tfj), uu = __uint_as_float(p1[jj]) * (f1 * tfj);
+      const float v0 = silu_f(gg) * uu;
+      overflow |= !(fabsf(v0) < 65520.f);  // f16 rounds these to inf
+      // h panels of 64 features: panel 2 nb0 + f / 64, row dst (the sorted row)
+      const int64_t panel = 2 * un.nb0 + (f >> 6);
+      *reinterpret_cast<__half*>(static_cast<uint8_t*>(a.out) + panel * a.act_rows * 128 +
+                                 static_cast<int64_t>(dst) * 128 + (f & 63) * 2) = __float2half_rn(v0);
+    } else {
+      __half* orow = static_cast<__half*>(a.out) + static_cast<int64_t>(dst) * a.n_nb * 128;
+      const float v0 = __uint_as_float(p0[jj]) * (f0 * tfj);
+      overflow |= !(fabsf(v0) < 65520.f);
+      orow[un.nb0 * 128 + f] = __float2half_rn(v0);
+      if (has1) {
+        const float v1 = __uint_as_float(p1[jj]) * (f1 * tfj);
+        overflow |= !(fabsf(v1) < 65520.f);
+        orow[un.nb1 * 128 + f] = __float2half_rn(v1);
       }
     }
-    __syncwarp();
   }
   if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(a.err, DEV_ERR_RANGE);
   return true;
@@ -317,24 +312,25 @@ __device__ __forceinline__ void regs_inc_epi() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
 }
 
-template <bool GATEUP, int WST, int TST>
+template <bool GATEUP>
 __global__ void __launch_bounds__(kThreadsF, 1)
 moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                     const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_tok32,
                     const __grid_constant__ CUtensorMap tm_tok64, const __grid_constant__ CUtensorMap tm_tok96,
                     const F16Args a) {
-  using C = F16Cfg<WST, TST>;
+  using C = F16Cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::kBarOff;
+  constexpr int WM = C::kWMax, TM = C::kTMax;
   auto full_w = [&](int i) { return bar0 + 8u * i; };
-  auto empty_w = [&](int i) { return bar0 + 8u * (WST + i); };
-  auto full_t = [&](int i) { return bar0 + 8u * (2 * WST + i); };
-  auto empty_t = [&](int i) { return bar0 + 8u * (2 * WST + TST + i); };
-  auto afull = [&](int i) { return bar0 + 8u * (2 * WST + 2 * TST + i); };
-  auto aempty = [&](int i) { return bar0 + 8u * (2 * WST + 2 * TST + kAStages + i); };
-  const uint32_t dfull = bar0 + 8u * (2 * WST + 2 * TST + 2 * kAStages);
+  auto empty_w = [&](int i) { return bar0 + 8u * (WM + i); };
+  auto full_t = [&](int i) { return bar0 + 8u * (2 * WM + i); };
+  auto empty_t = [&](int i) { return bar0 + 8u * (2 * WM + TM + i); };
+  auto afull = [&](int i) { return bar0 + 8u * (2 * WM + 2 * TM + i); };
+  auto aempty = [&](int i) { return bar0 + 8u * (2 * WM + 2 * TM + kAStages + i); };
+  const uint32_t dfull = bar0 + 8u * (2 * WM + 2 * TM + 2 * kAStages);
   const uint32_t dempty = dfull + 8u;
   const uint32_t drain_bar = bar0 + 8u * (C::kNumBars - 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + C::kNumBars * 8);
@@ -342,11 +338,11 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < WST; ++i) {
+    for (int i = 0; i < WM; ++i) {
       mbar_init(full_w(i), 1);
       mbar_init(empty_w(i), 4);  // the four converter warps
     }
-    for (int i = 0; i < TST; ++i) {
+    for (int i = 0; i < TM; ++i) {
       mbar_init(full_t(i), 1);
       mbar_init(empty_t(i), 1);  // one MMA commit
     }
@@ -381,7 +377,10 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
 
   const int n_nb = a.n_nb, num_kb = a.num_kb;
   const int upt = a.pair ? (n_nb + 1) / 2 : n_nb;  // units per tile
-  const int total_units = *a.n_tiles * upt;
+  const int total_units = a.n_tiles[0] * upt;
+  // the stage split (set with the tile list): weight stages 3 (w3) or 2, token stages the rest
+  const bool w3 = a.n_tiles[2] == 0;
+  const uint32_t tbase = sbase + (w3 ? 3 : 2) * kWStageF;
   // tiled layout: K block kb of unit row ru of expert e, both blocks (32 KB)
   auto unit_off = [&](int e, int ru, int kb) {
     return ((static_cast<int64_t>(e) * upt + ru) * num_kb + kb) * kWStageF;
@@ -399,8 +398,9 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
         const UnitF un = unit_f(a, u, upt);
         const uint64_t pol_w = un.reuse > 1 ? pol_shared : pol_once;
         for (int kb = 0; kb < num_kb; ++kb) {
-          const int sw = wi % WST;
-          if (!wait_bounded(empty_w(sw), ((wi / WST) & 1) ^ 1, abort_flag, a.err)) {
+          uint32_t pw;
+          const int sw = ring_stage<3, 2>(wi, w3, pw);
+          if (!wait_bounded(empty_w(sw), pw ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
@@ -416,8 +416,14 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
           ++wi;
         }
       }
-      if (!ok)
-        for (uint32_t i = wi > WST ? wi - WST : 0; i < wi; ++i) wait_drain_f(full_w(i % WST), (i / WST) & 1);
+      if (!ok) {
+        const uint32_t nw = w3 ? 3u : 2u;  // copies possibly in flight: the ring's last uses
+        for (uint32_t i = wi > nw ? wi - nw : 0; i < wi; ++i) {
+          uint32_t pw;
+          const int sw = ring_stage<3, 2>(i, w3, pw);
+          wait_drain_f(full_w(sw), pw);
+        }
+      }
     }
     __syncwarp();
   } else if (warp == kWarpTok) {
@@ -435,41 +441,50 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
         const int rb = box_rows_of(un.nv);
         const CUtensorMap* tm = rb == 32 ? &tm_tok32 : rb == 64 ? &tm_tok64 : rb == 96 ? &tm_tok96 : &tm_tok;
         for (int kb = 0; kb < num_kb; ++kb) {
-          const int st = ti % TST;
-          if (!wait_bounded(empty_t(st), ((ti / TST) & 1) ^ 1, abort_flag, a.err)) {
+          uint32_t pt;
+          const int st = ring_stage<4, 5>(ti, w3, pt);
+          if (!wait_bounded(empty_t(st), pt ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
-          const uint32_t dst = sbase + C::kTOff + st * kTStage;
+          const uint32_t dst = tbase + st * kTStage;
           mbar_arrive_expect_tx(full_t(st), rb * 256);
           tma_load_3d(dst, tm, full_t(st), 0, un.row0, 2 * kb, pol_t);  // panels 2 kb and 2 kb + 1
           ++ti;
         }
       }
-      if (!ok)
-        for (uint32_t i = ti > TST ? ti - TST : 0; i < ti; ++i) wait_drain_f(full_t(i % TST), (i / TST) & 1);
+      if (!ok) {
+        const uint32_t nt = w3 ? 4u : 5u;
+        for (uint32_t i = ti > nt ? ti - nt : 0; i < ti; ++i) {
+          uint32_t pt;
+          const int st = ring_stage<4, 5>(i, w3, pt);
+          wait_drain_f(full_t(st), pt);
+        }
+      }
     }
     __syncwarp();
   } else if (warp == kWarpMmaF) {
-    // The whole warp runs the loop (descriptors stay warp-uniform); one elected thread issues
-    // the MMAs and their commits.
-    uint32_t it = 0, ui = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
-      const UnitF un = unit_f(a, u, upt);
-      const int n_mma = (max(un.nv, 1) + 15) & ~15;  // N: the tile's rows, a multiple of 16
-      const uint32_t idesc = idesc_f16_f32(128, n_mma);
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
-        const int st = it % TST, sa = it % kAStages;
-        // the first K block overwrites the accumulators: they must have been read out
-        ok = __all_sync(0xffffffffu, (kb != 0 || wait_bounded(dempty, (ui & 1) ^ 1, abort_flag, a.err)) &&
-                                         wait_bounded(full_t(st), (it / TST) & 1, abort_flag, a.err) &&
-                                         wait_bounded(afull(sa), (it / kAStages) & 1, abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tb = sbase + C::kTOff + st * kTStage;
-        const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + box_rows_of(un.nv) * 128);
-        if (elect_one()) {
+    // One elected thread runs the whole loop: its waits, MMAs and commits.
+    if (elect_one()) {
+      uint32_t it = 0, ui = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++ui) {
+        const UnitF un = unit_f(a, u, upt);
+        const int n_mma = (max(un.nv, 1) + 15) & ~15;  // N: the tile's rows, a multiple of 16
+        const uint32_t idesc = idesc_f16_f32(128, n_mma);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          uint32_t pt;
+          const int st = ring_stage<4, 5>(it, w3, pt), sa = it % kAStages;
+          // the first K block overwrites the accumulators: they must have been read out
+          if ((kb == 0 && !wait_bounded(dempty, (ui & 1) ^ 1, abort_flag, a.err)) ||
+              !wait_bounded(full_t(st), pt, abort_flag, a.err) ||
+              !wait_bounded(afull(sa), (it / kAStages) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tb = tbase + st * kTStage;
+          const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + box_rows_of(un.nv) * 128);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             if (m == 1 && !un.has1) break;
@@ -484,12 +499,10 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
           tc_commit(aempty(sa));
           if (kb == num_kb - 1) tc_commit(dfull);
         }
-        __syncwarp();
       }
+      tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
+      wait_drain_f(drain_bar, 0);
     }
-    if (elect_one()) tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
-    __syncwarp();
-    wait_drain_f(drain_bar, 0);
     __syncwarp();
   } else if (warp >= kWarpConv && warp < kWarpEpi) {
     // converters: weight row r of both blocks, K block by K block, into the A stages
@@ -505,11 +518,12 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
       b0.load(a.s0 + (static_cast<int64_t>(un.e) * n_nb + un.nb0) * num_kb, num_kb, lane);
       b1.load(a.s1 + (static_cast<int64_t>(un.e) * n_nb + (un.has1 ? un.nb1 : un.nb0)) * num_kb, num_kb, lane);
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
-        const int sw = it % WST, sa = it % kAStages;
+        uint32_t pw;
+        const int sw = ring_stage<3, 2>(it, w3, pw), sa = it % kAStages;
         const float s0v = b0.at(kb), s1v = b1.at(kb);
         // Every lane waits (each gets the barrier's acquire); the vote keeps the warp
         // converged for the .sync.aligned tensor-memory stores.
-        ok = __all_sync(0xffffffffu, wait_bounded(full_w(sw), (it / WST) & 1, abort_flag, a.err) &&
+        ok = __all_sync(0xffffffffu, wait_bounded(full_w(sw), pw, abort_flag, a.err) &&
                                          wait_bounded(aempty(sa), ((it / kAStages) & 1) ^ 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
@@ -543,7 +557,6 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
     pdl_wait();  // token scales, positions and router weights come from earlier kernels
     const int q = warp & 3;
     const int half = (warp - kWarpEpi) >> 2;
-    uint8_t* wbuf = smem + C::kBufOff + (warp - kWarpEpi) * kStageBufBytes;
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++ui) {
       const UnitF un = unit_f(a, u, upt);
@@ -555,7 +568,7 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
         m1 = fmaxf(m1, __ldg(sc1 + kb));
       }
       const int cw0 = pow2_of_max(m0), cw1 = pow2_of_max(m1);
-      if (!unit_epilogue<GATEUP>(a, un, cw0, cw1, ui, tmem, q, half, dfull, dempty, abort_flag, wbuf)) break;
+      if (!unit_epilogue<GATEUP>(a, un, cw0, cw1, ui, tmem, q, half, dfull, dempty, abort_flag)) break;
     }
   }
   __syncthreads();
@@ -565,10 +578,10 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
   }
 }
 
-template <bool GATEUP, int WST, int TST>
+template <bool GATEUP>
 cudaError_t launch_f16(const GemmLaunch& g, cudaStream_t s) {
-  using C = F16Cfg<WST, TST>;
-  auto kern = moe_gemm_f16_kernel<GATEUP, WST, TST>;
+  using C = F16Cfg;
+  auto kern = moe_gemm_f16_kernel<GATEUP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   if (!g.act_box || !g.act_box_rows[0] || !g.act_box_rows[1] || !g.act_box_rows[2]) return cudaErrorInvalidValue;
@@ -600,17 +613,15 @@ cudaError_t launch_f16(const GemmLaunch& g, cudaStream_t s) {
 
 }  // namespace
 
-// Stages: three 32 KB weight stages (both blocks of one K block; released as soon
-// as they are converted) and three 32 KB token stages (128 rows x 128 f16, one
-// TMA box each), plus 8 KB of epilogue transpose buffers; 201 KB of shared
-// memory.  What bounds the K-block period (measured with timestamps and copy
-// probes): a stage is reissued only when its previous contents are consumed, and
-// while an SM streams weights from DRAM its token boxes (L2 hits, ~840 cycles
-// alone) take as long as the weight copies, ~3,700-4,200 cycles; with three
-// stages a side the period is about (that latency + the stage's hold time) / 3,
-// ~1,750 cycles against ~1,050 of MMA issue.  More stages do not fit; an L2
-// prefetch of the weights ahead of their copies did not shorten the period.
-cudaError_t launch_gateup_f16(const GemmLaunch& g, cudaStream_t s) { return launch_f16<true, 3, 3>(g, s); }
-cudaError_t launch_down_f16(const GemmLaunch& g, cudaStream_t s) { return launch_f16<false, 3, 3>(g, s); }
+// Stages: seven 32 KB operand stages (F16Cfg), three for weights (both blocks of
+// one K block; released as soon as they are converted) and four for tokens (128
+// rows x 128 f16, one TMA box each), or two and five when the tile list marks its
+// weights as shared; 225 KB of shared memory.  What bounds the K-block period
+// (timestamps, copy probes, timing-only knock-outs): with one tile per expert
+// the weight stream from DRAM (the gate/up pass reaches the copy bandwidth);
+// with several tiles per expert the tensor pipe and the token stream, whose
+// boxes queue behind the SM's weight copies (~3,000 cycles from issue to use).
+cudaError_t launch_gateup_f16(const GemmLaunch& g, cudaStream_t s) { return launch_f16<true>(g, s); }
+cudaError_t launch_down_f16(const GemmLaunch& g, cudaStream_t s) { return launch_f16<false>(g, s); }
 
 }  // namespace moe

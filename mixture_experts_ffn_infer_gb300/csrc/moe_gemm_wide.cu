@@ -29,7 +29,7 @@
 //   0      weight producer: the K block's two 16 KB tiles (one 32 KB bulk copy
 //          of the tiled layout, or 3-D TMA of the row-major layout), and an L2
 //          prefetch ahead when several token tiles share an expert's weights
-//   1      MMA issuer (the warp runs the loop, one elected thread issues)
+//   1      MMA issuer (one thread, elected)
 //   2      activation producer: one TMA box [128 rows][128 bytes] per K block
 //   3      idle
 //   4..11  epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (the
@@ -304,25 +304,26 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
     }
     __syncwarp();
   } else if (warp == kWarpIssue) {
-    // The whole warp runs the loop (descriptors stay warp-uniform); one elected thread issues
-    // the MMAs and their commits.
-    uint32_t it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const Unit un = unit_of(a, u, upt);
-      // kind::f8f6f4 with E4M3 operands: format code 0, the same bits as f16
-      const uint32_t idesc = idesc_f16_f32(128, un.has1 ? 256 : 128);
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
-        const int sw = it % WST, sa = it % AST, sd = it & 1;
-        ok = __all_sync(0xffffffffu, wait_bounded(full_w(sw), (it / WST) & 1, abort_flag, a.err) &&
-                                         wait_bounded(full_a(sa), (it / AST) & 1, abort_flag, a.err) &&
-                                         wait_bounded(dempty(sd), ((it >> 1) & 1) ^ 1, abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t wdesc = desc_kmajor_sw128(sbase + sw * C::kWStage);
-        const uint64_t adesc = desc_kmajor_sw128(sbase + C::kAOff + sa * C::kAStage);
-        const uint32_t d = tmem + static_cast<uint32_t>(sd) * 256;
-        if (elect_one()) {
+    // One elected thread runs the whole loop: its waits, MMAs and commits.
+    if (elect_one()) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit un = unit_of(a, u, upt);
+        // kind::f8f6f4 with E4M3 operands: format code 0, the same bits as f16
+        const uint32_t idesc = idesc_f16_f32(128, un.has1 ? 256 : 128);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int sw = it % WST, sa = it % AST, sd = it & 1;
+          if (!wait_bounded(full_w(sw), (it / WST) & 1, abort_flag, a.err) ||
+              !wait_bounded(full_a(sa), (it / AST) & 1, abort_flag, a.err) ||
+              !wait_bounded(dempty(sd), ((it >> 1) & 1) ^ 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t wdesc = desc_kmajor_sw128(sbase + sw * C::kWStage);
+          const uint64_t adesc = desc_kmajor_sw128(sbase + C::kAOff + sa * C::kAStage);
+          const uint32_t d = tmem + static_cast<uint32_t>(sd) * 256;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8(d, desc_advance(adesc, kk * 32), desc_advance(wdesc, kk * 32), idesc, kk > 0 ? 1u : 0u);
@@ -330,12 +331,10 @@ moe_gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_con
           tc_commit(empty_a(sa));
           tc_commit(dfull(sd));
         }
-        __syncwarp();
       }
+      tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
+      wait_drain_w(drain_bar, 0);
     }
-    if (elect_one()) tc_commit(drain_bar);  // every MMA issued above has completed once this arrives
-    __syncwarp();
-    wait_drain_w(drain_bar, 0);
     __syncwarp();
   } else if (warp >= kWarpEpi) {
     regs_inc_epilogue();

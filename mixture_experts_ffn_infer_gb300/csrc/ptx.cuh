@@ -113,13 +113,13 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// True on one thread of a converged warp and false on the others.  For a full member mask the
-// same lane is elected every time (elect.sync's election is deterministic), so that thread's
-// tcgen05.commit tracks every MMA issued under the same election.  Issuing MMAs from a
-// converged warp this way keeps their operands warp-uniform: measured on every SM, one
-// kind::f16 MMA (M 128, K 16, A in tensor memory) then costs what the tensor pipe needs
-// (35 cycles at N 32 rising to 70 at N 128), against a flat ~71-75 cycles when a lone
-// thread issues it from a lane-0 branch.
+// True on one thread of a converged warp and false on the others (for a full
+// member mask the same lane every time).  A lone thread that runs an MMA loop
+// inside an elect_one() region issues at the tensor pipe's pace: measured on
+// every SM, one kind::f16 MMA (M 128, K 16, A in tensor memory) then costs 29
+// cycles at N 32 rising to 64 at N 128, against a flat ~71 cycles when the same
+// loop runs in a lane-0 branch, and 35-70 when the whole warp runs the loop and
+// elects the issuing thread per K block.
 __device__ __forceinline__ bool elect_one() {
   uint32_t e;
   asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(e));

@@ -61,16 +61,22 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 }
 
 // Tiles of at most ntok rows over every expert's slice [offsets[e], offsets[e+1]),
-// in expert order; the whole CTA (kThreads threads) takes part.
+// in expert order; the whole CTA (kThreads threads) takes part.  n_tiles[0] gets
+// the tile count, n_tiles[2] the weight-sharing flag (tiles_share_weights).
 __device__ void cta_build_tiles(const int32_t* __restrict__ offsets, int E, int ntok, TileDesc* __restrict__ tiles,
                                 int32_t* __restrict__ n_tiles, int* warp_sums) {
   const int tid = threadIdx.x;
   const int per = (E + kThreads - 1) / kThreads;
   const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
-  int local = 0;
-  for (int e = e0; e < e1; ++e) local += (offsets[e + 1] - offsets[e] + ntok - 1) / ntok;
-  int total;
+  int local = 0, local_multi = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int nt_e = (offsets[e + 1] - offsets[e] + ntok - 1) / ntok;
+    local += nt_e;
+    if (nt_e >= 2) local_multi += nt_e;
+  }
+  int total, multi;
   int t = block_exclusive_scan(local, warp_sums, &total);
+  block_exclusive_scan(local_multi, warp_sums, &multi);
   for (int e = e0; e < e1; ++e) {
     const int beg = offsets[e], end = offsets[e + 1];
     const int nt_e = (end - beg + ntok - 1) / ntok;
@@ -79,7 +85,10 @@ __device__ void cta_build_tiles(const int32_t* __restrict__ offsets, int E, int 
       tiles[t++] = TileDesc{e, r, min(ntok, end - r), tile_chunk_code(i, nt_e)};
     }
   }
-  if (tid == 0) *n_tiles = total;
+  if (tid == 0) {
+    n_tiles[0] = total;
+    n_tiles[2] = tiles_share_weights(multi, total);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -314,7 +323,10 @@ __global__ void identity_tiles_kernel(int32_t rows, int32_t ntok, TileDesc* tile
   const int nt = (rows + ntok - 1) / ntok;
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nt; t += gridDim.x * blockDim.x)
     tiles[t] = TileDesc{0, t * ntok, min(ntok, rows - t * ntok), tile_chunk_code(t, nt)};
-  if (blockIdx.x == 0 && threadIdx.x == 0) *n_tiles = nt;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    n_tiles[0] = nt;
+    n_tiles[2] = tiles_share_weights(nt >= 2 ? nt : 0, nt);  // one expert: every tile shares its weights
+  }
 }
 
 // One thread waits on a barrier that nothing completes, through the same bounded
