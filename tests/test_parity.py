@@ -145,6 +145,40 @@ def test_forced_empty_experts_and_hot_expert():
     _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank), ref)
 
 
+def _tile_split_flag(counts, tile=128):
+    """The stage-split rule of the wide f16 GEMM: 1 when at least 90 % of the tiles belong to
+    experts cut into two or more tiles."""
+    tiles = [(c + tile - 1) // tile for c in counts]
+    multi = sum(t for t in tiles if t >= 2)
+    return int(sum(tiles) > 0 and 10 * multi >= 9 * sum(tiles)), sum(tiles)
+
+
+@pytest.mark.parametrize("counts", [
+    [200, 200, 200, 200, 129, 50, 0, 0],   # 10 of 11 tiles in multi-tile experts: 2 + 5 stages
+    [200, 200, 200, 200, 50, 50, 0, 0],    # 8 of 10: 3 + 4
+    [100] * 8,                             # one tile per expert
+    [1300, 20, 0, 0, 0, 0, 0, 0],          # a hot expert: 11 of 12
+])
+def test_wide_stage_split_flag_and_parity(counts):
+    # Wide tiles (128 rows, d 1024: 8 K blocks per gate/up unit, so either ring wraps) with a
+    # chosen number of tiles per expert.  The routing kernel writes the tile count and the
+    # weight-sharing flag to the workspace words at bytes 64 and 72; both stage splits must
+    # give the oracle's output.
+    E, n = 8, sum(counts)
+    wl = syn.Workload("split", n, 1024, 256, E, 1, seed=21)
+    g = torch.Generator().manual_seed(5)
+    ids = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(counts)])
+    ids = ids[torch.randperm(n, generator=g)].reshape(n, 1).contiguous()
+    c = cases.workload(wl, ids=ids)
+    c.ids = ids.cuda()
+    ws = mx.workspace(mx.dims(1024, 256, E, 1), n)
+    y = mx.infer(c.x, c.ids, c.w, c.bank, ws=ws)
+    words = ws[64:80].view(torch.int32).cpu().tolist()
+    flag, n_tiles = _tile_split_flag(counts)
+    assert words[0] == n_tiles and words[2] == flag, (words, n_tiles, flag)
+    _assert_ok(y, oracle.moe_infer(c.inp.x, ids, c.inp.topk_weight, c.inp.bank))
+
+
 # ------------------------------------------------------------------ K2 sizes
 
 def test_k2_decode_whole_output():
