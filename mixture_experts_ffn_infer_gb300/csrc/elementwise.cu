@@ -130,11 +130,14 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint16_t
 
 // One CTA per token: the row's largest magnitude, then the row as f16 times
 // 2^-s to every sorted position of the token, and 2^s to the factor array.
+// Each thread moves 8 columns at a time (16-byte loads and stores) and keeps
+// its first kHeld groups in registers between the two passes.
 __global__ void __launch_bounds__(kRowThreads) gather_rows_f16_kernel(const uint16_t* __restrict__ x,
                                                                       const int32_t* __restrict__ inv_pos,
                                                                       int32_t n, int32_t k, int32_t d,
                                                                       uint8_t* __restrict__ xs, SplitLayout lay,
                                                                       float* __restrict__ xs_scale) {
+  constexpr int kHeld = 4;  // rows up to 8 * kRowThreads * kHeld = 8192 columns are read once
   __shared__ float red[kRowThreads / 32];
   pdl_wait();  // launched behind the routing plan, whose inv_pos it reads
   pdl_launch_dependents();
@@ -147,22 +150,41 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_f16_kernel(const uint
     if (p >= 0 && p < R) dst_rows[ndst++] = p;
   }
   if (ndst == 0) return;  // the whole CTA leaves together (ndst is the same for every thread)
-  const uint2* src = reinterpret_cast<const uint2*>(x + t * d);  // four bf16 per uint2
-  const int nq = d / 4;
+  const uint4* src = reinterpret_cast<const uint4*>(x + t * d);  // eight bf16 per uint4
+  const int n8 = d / 8;
+  auto max8 = [](const uint4& w) {
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(q[i])), fabsf(bf16_hi(q[i]))));
+    return m;
+  };
+  uint4 held[kHeld];
   float m = 0.f;
-  for (int c = threadIdx.x; c < nq; c += kRowThreads) {
-    const uint2 w = src[c];
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))), fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
+#pragma unroll
+  for (int i = 0; i < kHeld; ++i) {
+    const int c = threadIdx.x + i * kRowThreads;
+    held[i] = c < n8 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+    m = fmaxf(m, max8(held[i]));
   }
+  for (int c = threadIdx.x + kHeld * kRowThreads; c < n8; c += kRowThreads) m = fmaxf(m, max8(src[c]));
   const int s = f16_row_exponent(block_max(m, red));
-  for (int c = threadIdx.x; c < nq; c += kRowThreads) {
-    const uint2 w = src[c];
-    const float v[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
-    const uint2 o = f16x4_scaled(v, s);
-    // columns 4c..4c+3: panel c / 16, bytes (c % 16) * 8 of the row's 128 in it
-    uint8_t* panel = xs + static_cast<int64_t>(c >> 4) * lay.term_stride + (c & 15) * 8;
-    for (int q = 0; q < ndst; ++q) *reinterpret_cast<uint2*>(panel + static_cast<int64_t>(dst_rows[q]) * lay.row_stride) = o;
+  // columns 8c..8c+7: panel c / 8, bytes (c % 8) * 16 of the row's 128 in it
+  auto store8 = [&](int c, const uint4& w) {
+    const float v0[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+    const float v1[4] = {bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+    const uint2 a = f16x4_scaled(v0, s), b = f16x4_scaled(v1, s);
+    const uint4 o = make_uint4(a.x, a.y, b.x, b.y);
+    uint8_t* panel = xs + static_cast<int64_t>(c >> 3) * lay.term_stride + (c & 7) * 16;
+    for (int q = 0; q < ndst; ++q)
+      *reinterpret_cast<uint4*>(panel + static_cast<int64_t>(dst_rows[q]) * lay.row_stride) = o;
+  };
+#pragma unroll
+  for (int i = 0; i < kHeld; ++i) {
+    const int c = threadIdx.x + i * kRowThreads;
+    if (c < n8) store8(c, held[i]);
   }
+  for (int c = threadIdx.x + kHeld * kRowThreads; c < n8; c += kRowThreads) store8(c, src[c]);
   if (threadIdx.x < ndst) xs_scale[dst_rows[threadIdx.x]] = ldexpf(1.0f, s);
 }
 
