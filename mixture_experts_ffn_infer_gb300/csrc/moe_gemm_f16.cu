@@ -40,17 +40,20 @@
 //
 // Warps (512 threads = 4 warpgroups, one CTA per SM, persistent over the unit
 // list; warpgroups 0 and 1 hand registers to the epilogue warpgroups):
-//   0      weight producer: one 32 KB copy per K block (both tiles)
+//   0      weight producer: one 32 KB copy per K block (both tiles) into the
+//          weight ring (3 stages, or 2 when the tile list marks its weights as
+//          shared by the experts' several tiles)
 //   1      MMA issuer (one thread, elected)
 //   2      token producer: one TMA box [2 panels][rows][64 f16] per K block, the
-//          tile's rows rounded up to 32
+//          tile's rows rounded up to 32, into the token ring (4 or 5 stages)
 //   3      idle
 //   4..7   converters: warp 4 + q owns tensor-memory lanes 32q..32q+31, i.e.
 //          weight row 32q + lane of both blocks
 //   8..15  epilogue: warp w reads lanes 32 (w % 4).. (output features) and
 //          tokens 64 ((w - 8) / 4) .. +63 of both accumulators with one wait,
 //          releases them (the next unit's MMAs start) and forms and writes its
-//          outputs while the next unit's K blocks are converted and multiplied.
+//          outputs (straight from registers, a 64-byte store per token) while
+//          the next unit's K blocks are converted and multiplied.
 //
 // Every wait is bounded; a wait that gives up raises the abort flag and the
 // device error word, and every role drains what it has in flight before the
