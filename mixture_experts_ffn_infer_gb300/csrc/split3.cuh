@@ -60,24 +60,6 @@ __device__ __forceinline__ void split3x4(const float (&v)[4], int s, uint32_t& t
   }
 }
 
-// 2^k for -126 <= k <= 127, exactly.
-__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
-
-// Two already-scaled values (|v| < 448) -> their e4m3 codes of each term, as
-// byte pairs (first value in the low byte): the same rounding steps as split3.
-__device__ __forceinline__ void split3_pair(float2 v, uint32_t& c1, uint32_t& c2, uint32_t& c3) {
-  const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-  const float2 av = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3)));
-  const float2 r1 = make_float2(v.x - av.x, v.y - av.y);
-  const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(r1, __NV_SATFINITE, __NV_E4M3);
-  const float2 bv = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(b, __NV_E4M3)));
-  const float2 r2 = make_float2(r1.x - bv.x, r1.y - bv.y);
-  const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(r2, __NV_SATFINITE, __NV_E4M3);
-  c1 = a;
-  c2 = b;
-  c3 = c;
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
