@@ -145,6 +145,15 @@ def test_forced_empty_experts_and_hot_expert():
     _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank), ref)
 
 
+def test_wide_tiles_rows_wider_than_the_gather_holds():
+    # d 8320 (65 K blocks): the f16 row gather keeps up to 8192 columns of a row in registers and
+    # reads the rest a second time; wide tiles (64 rows over 2 experts), 130 f16 panels per row
+    wl = syn.Workload("wide8320", 64, 8320, 128, 2, 1, seed=23)
+    c = cases.workload(wl)
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.inp.bank)
+    _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank), ref)
+
+
 def _tile_split_flag(counts, tile=128):
     """The stage-split rule of the wide f16 GEMM: 1 when at least 90 % of the tiles belong to
     experts cut into two or more tiles."""
