@@ -43,6 +43,13 @@ def _infer_ref(c, tokens=None, bank=None):
                             tokens=tokens, fp8_act=True)
 
 
+def test_fp8_wide_tiles_rows_of_8320_features():
+    # 65 K blocks through the dynamic FP8 gather and the FP8 wide-tile kernel
+    wl = syn.Workload("wide8320", 64, 8320, 128, 2, 1, seed=23)
+    c = cases.workload(wl)
+    _assert_ok(mx.infer(c.x, c.ids, c.w, c.bank, act_scheme=FP8), _infer_ref(c))
+
+
 def test_tiny_fp8_matches_oracle_and_scheme_accuracy():
     c = cases.workload("tiny")   # 32 rows per expert: wide tiles
     ref = _infer_ref(c)
