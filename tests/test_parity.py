@@ -212,6 +212,19 @@ def test_k2_large_sampled_tokens(name):
     assert torch.isfinite(y.float()).all()
 
 
+def test_k2_twice_the_block_batch_sampled_tokens():
+    # 65,536 tokens (R = 524,288 routed rows): element offsets into the sorted rows and the expert
+    # outputs pass 2^31, so any 32-bit index arithmetic on the wide-tile path would show here
+    wl = syn.Workload("k2_65536", 65536, 7168, 2048, 384, 8, seed=4, bank_seed=1)
+    c = cases.workload(wl)
+    y = mx.infer(c.x, c.ids, c.w, c.bank)
+    tok = cases.parity_tokens(c.inp.topk_ids, n_min=512, seed=3)
+    assert len(tok) >= 512 and tok[-1] == wl.n_tokens - 1
+    ref = oracle.moe_infer(c.inp.x, c.inp.topk_ids, c.inp.topk_weight, c.bank, tokens=tok)
+    _assert_ok(y[tok], ref)
+    assert torch.isfinite(y.float()).all()
+
+
 def test_k2_block_sampled_tokens():
     c = cases.workload("k2_block")
     y = mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, c.shared)
