@@ -123,6 +123,17 @@ def test_k2_large_fp8_sampled_tokens(name):
     assert torch.isfinite(y.float()).all()
 
 
+def test_k2_twice_the_block_batch_fp8_sampled_tokens():
+    # 65,536 tokens (R = 524,288 routed rows) through the dynamic FP8 gather and wide-tile kernel
+    wl = syn.Workload("k2_65536", 65536, 7168, 2048, 384, 8, seed=4, bank_seed=1)
+    c = cases.workload(wl)
+    y = mx.infer(c.x, c.ids, c.w, c.bank, act_scheme=FP8)
+    tok = cases.parity_tokens(c.inp.topk_ids, n_min=512, seed=3)
+    assert len(tok) >= 512 and tok[-1] == wl.n_tokens - 1
+    _assert_ok(y[tok], _infer_ref(c, tokens=tok, bank=c.bank))
+    assert torch.isfinite(y.float()).all()
+
+
 def test_k2_block_fp8_sampled_tokens():
     c = cases.workload("k2_block")
     y = mx.layer_forward(c.x, c.gain, c.inp.eps, c.ids, c.w, c.bank, c.shared, act_scheme=FP8)
